@@ -1,0 +1,433 @@
+"""Throughput benchmark of the batch-invariant selected-token logprob path.
+
+One step = one pass of the whole hot path on one GPU:
+  1. linear_logp forward (tile kernel + merge) on a GRPO group: 64 completions
+     x 1024 tokens (T = 65536), H = 4096, V = 128256, bf16, seeded synthetic data;
+  2. linear_logp backward (dZ GEMM + dh GEMM) on the same rows, g ~ N(0, 1);
+  3. the logits path on T = 2048 rows of V = 32000 bf16 logits (rotated over 4
+     buffers so that no call finds its input in L2).
+`value` = tokens (rows of the GRPO group, summed over ranks) per second of
+device time, inputs resident in HBM.  h (512 MB) and W (1.05 GB) exceed the
+126 MB L2, so nothing carries over between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own group (weak scaling, no data
+collective); the timed region is bracketed by barriers and the max over ranks
+is reported.  `--impl reference` times the fp64 CPU oracle on a bounded sample
+of the same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "linear_logp tokens/s & % BF16 tensor peak, bitwise batch-invariant"
+UNIT = "tokens/s"
+GRPO = dict(n_seqs=64, seq_len=1024, H=4096, V=128256)
+LOGITS = dict(T=2048, V=32000)
+N_LOGITS_BUFFERS = 4
+WORKLOAD = ("grpo_fwd_bwd: linear_logp fwd+bwd T=65536 (64x1024) H=4096 V=128256 bf16, "
+            "+ logits path T=2048 V=32000 bf16")
+
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of the tile kernel, per
+# launch, scaled to the full workload, recorded together with a hash of the
+# kernel source; reported only while the source still matches.
+TRAFFIC_RECORD = {"source_sha1": None, "fwd_tiles_bytes": None}
+
+
+def kernel_source_sha1() -> str:
+    p = os.path.join(ROOT, "invariant_rl_logprob_gb300", "csrc", "linear_logp_tc.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (weak scaling, timing max over ranks)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, world_size: int) -> float:
+    if world_size == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world_size: int) -> None:
+    if world_size > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="rk_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        loaded = [s for s in sm if s > 0.5 * smax] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for i, n in enumerate(names):
+                if r[5 + i].lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows
+                                    if r[3].replace(".", "").isdigit()), default=None)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+
+def make_inputs(rank: int):
+    from invariant_rl_logprob_gb300 import synth
+    seed_shift = 100 * rank
+    c = synth.WORKLOADS["grpo"]
+    lengths = [GRPO["seq_len"]] * GRPO["n_seqs"]
+    pool = synth.make_pool(GRPO["H"], GRPO["V"], lengths, c["seed"] + seed_shift, with_grad=True)
+    logits = []
+    for i in range(N_LOGITS_BUFFERS):
+        z, tg, _ = synth.logits_batch(seed=synth.WORKLOADS["logits"]["seed"] + seed_shift + 10 * i)
+        logits.append((z, tg))
+    return pool, logits
+
+
+def cpu_oracle_sample(pool, logits, n_rows: int) -> tuple[float, int, str]:
+    """Time the fp64 oracle (single thread) on n_rows GRPO rows (fwd + bwd) and
+    n_rows logits-path rows; returns (tokens/s, cores, description)."""
+    import numpy as np
+
+    import oracle
+    from invariant_rl_logprob_gb300 import synth
+    oracle.build()
+    hb = synth.bf16_bits(pool.h)
+    Wb = synth.bf16_bits(pool.W)
+    tg = pool.targets.numpy()
+    g = pool.g.double().numpy()
+    rows = synth.sample_rows(pool.h.shape[0], n_rows, seed=4)
+    zb = synth.bf16_bits(logits[0][0])
+    ztg = logits[0][1].numpy()
+    zrows = synth.sample_rows(zb.shape[0], n_rows, seed=1)
+    t0 = time.perf_counter()
+    oracle.linear_logp(hb, Wb, tg, rows=rows)
+    oracle.linear_logp_bwd(hb, Wb, tg, g, rows=rows)
+    oracle.logp_from_logits(zb, ztg, rows=zrows)
+    dt = time.perf_counter() - t0
+    # one GRPO row of the step carries 2048/65536 of a logits-path row with it;
+    # the logits rows are timed in full and charged to the same token count
+    desc = (f"{n_rows} GRPO rows (fwd + bwd, H=4096, V=128256) + {n_rows} logits-path rows "
+            f"(V=32000), fp64 oracle, 1 thread, {dt:.1f} s")
+    return n_rows / dt, 1, desc
+
+
+def run_reference(args) -> None:
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from invariant_rl_logprob_gb300 import synth
+    c = synth.WORKLOADS["grpo"]
+    # only W and a handful of rows are needed on the host
+    lengths = [GRPO["seq_len"]] * GRPO["n_seqs"]
+    pool = synth.make_pool(GRPO["H"], GRPO["V"], lengths, c["seed"], with_grad=True)
+    z, ztg, _ = synth.logits_batch()
+    logits = [(z, ztg)]
+    rows_per_step = 1
+    times = []
+    for i in range(args.warmup + args.steps):
+        v, cores, desc = cpu_oracle_sample(pool, logits, rows_per_step)
+        if i >= args.warmup:
+            times.append(rows_per_step / v)
+    ms = 1000.0 * statistics.mean(times)
+    value = rows_per_step / (ms / 1000.0)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": f"{rows_per_step} GRPO row(s) fwd+bwd + "
+                   f"{rows_per_step} logits-path row(s) per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args) -> None:
+    import torch
+
+    import invariant_rl_logprob_gb300 as rk
+    from invariant_rl_logprob_gb300 import build as rk_build
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0 or ws == 1:
+        rk_build.build()
+    barrier(ws)
+    rk.load_library()
+    peaks = load_peaks()
+
+    pool, logits_host = make_inputs(rank)
+    T, H, V = pool.h.shape[0], pool.H, pool.V
+    Tl, Vl = LOGITS["T"], LOGITS["V"]
+    stream = torch.cuda.current_stream(dev)
+
+    h = pool.h.to(dev)
+    W = pool.W.to(dev)
+    tg = pool.targets.to(dev)
+    g = pool.g.to(dev)
+    zs = [(z.to(dev), t.to(dev)) for z, t in logits_host]
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    dh = torch.empty((T, H), dtype=torch.float32, device=dev)
+    zlogp = torch.empty(Tl, dtype=torch.float32, device=dev)
+    zlse = torch.empty(Tl, dtype=torch.float32, device=dev)
+    ws_fwd = torch.empty(rk.linear_logp_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
+    ws_bwd = torch.empty(rk.linear_logp_bwd_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
+    bwd_chunks = 1   # the full workspace holds every row: one dZ GEMM + one dh GEMM
+    launches_per_step = 2 + (2 * bwd_chunks + 1) + 1
+
+    def step(i):
+        rk.linear_logp(h, W, tg, out=logp, lse=lse, workspace=ws_fwd, stream=stream)
+        rk.linear_logp_bwd(h, W, tg, lse, g, dh=dh, workspace=ws_bwd, stream=stream)
+        z, zt = zs[i % len(zs)]
+        rk.logp_from_logits(z, zt, out=zlogp, lse=zlse, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    err = rk.get_device_error(stream)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        t_wall = time.perf_counter()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            e = ev[i]
+            e[0].record(stream)
+            rk.linear_logp(h, W, tg, out=logp, lse=lse, workspace=ws_fwd, stream=stream)
+            e[1].record(stream)
+            rk.linear_logp_bwd(h, W, tg, lse, g, dh=dh, workspace=ws_bwd, stream=stream)
+            e[2].record(stream)
+            z, zt = zs[(args.warmup + i) % len(zs)]
+            rk.logp_from_logits(z, zt, out=zlogp, lse=zlse, stream=stream)
+            e[3].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t_wall
+    barrier(ws)
+    total_ms = start.elapsed_time(end)
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    lg_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
+    err = rk.get_device_error(stream)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} in the timed region")
+
+    ms_step_local = total_ms / args.steps
+    ms_step = max_over_ranks(ms_step_local, ws)
+    value = ws * T / (ms_step / 1000.0)
+
+    # ---- end to end: host buffers in, results out, through the public API ----
+    pin = lambda t: t.pin_memory()
+    h_h, W_h, tg_h, g_h = pin(pool.h), pin(pool.W), pin(pool.targets), pin(pool.g)
+    z_h = [(pin(z), pin(t)) for z, t in logits_host]
+    dh_h = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    logp_h = torch.empty(T, dtype=torch.float32).pin_memory()
+    zlogp_h = torch.empty(Tl, dtype=torch.float32).pin_memory()
+    h2d = (h_h.numel() * 2 + W_h.numel() * 2 + tg_h.numel() * 8 + g_h.numel() * 4
+           + Tl * Vl * 2 + Tl * 8)
+    d2h = dh_h.numel() * 4 + logp_h.numel() * 4 + zlogp_h.numel() * 4
+
+    def e2e_step(i):
+        h.copy_(h_h, non_blocking=True)
+        W.copy_(W_h, non_blocking=True)
+        tg.copy_(tg_h, non_blocking=True)
+        g.copy_(g_h, non_blocking=True)
+        z, zt = zs[i % len(zs)]
+        zh, zth = z_h[i % len(z_h)]
+        z.copy_(zh, non_blocking=True)
+        zt.copy_(zth, non_blocking=True)
+        step(i)
+        dh_h.copy_(dh, non_blocking=True)
+        logp_h.copy_(logp, non_blocking=True)
+        zlogp_h.copy_(zlogp, non_blocking=True)
+
+    for i in range(min(args.warmup, 2)):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    s2 = torch.cuda.Event(enable_timing=True)
+    e2 = torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e2.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2) / args.steps, ws)
+    e2e_value = ws * T / (e2e_ms / 1000.0)
+
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    flops_fwd = 2.0 * T * H * V
+    flops_bwd = 4.0 * T * H * V
+    tc_tflops = (flops_fwd + flops_bwd) / ((fwd_ms + bwd_ms) / 1000.0) / 1e12
+    peak_tc = peaks["bf16_tflops_sustained"]
+    lg_bytes = Tl * Vl * 2 + Tl * 8 + 2 * Tl * 4
+    lg_gbs = lg_bytes / (lg_ms / 1000.0) / 1e9
+    traffic = None
+    if TRAFFIC_RECORD["source_sha1"] == kernel_source_sha1():
+        traffic = TRAFFIC_RECORD["fwd_tiles_bytes"]
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, cores, desc = cpu_oracle_sample(pool, logits_host, args.cpu_rows)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": ws * T, "seq_len": GRPO["seq_len"],
+                   "H": H, "V": V, "parallelism": f"replicas x{ws}" if ws > 1 else "single",
+                   "l2": "inputs larger than L2 (h 512 MB, W 1.05 GB); logits rotated over "
+                         f"{N_LOGITS_BUFFERS} buffers of {Tl * Vl * 2 / 1e6:.0f} MB"},
+        "roofline": {"bound": "tensor", "achieved": tc_tflops, "peak": peak_tc,
+                     "unit": "TFLOP/s", "frac": tc_tflops / peak_tc, "traffic": traffic,
+                     "kernel": "linear_logp_tiles (fwd + dZ + dh launches; each timed with the "
+                               "small kernels of its call)",
+                     "algorithmic": "6*T*H*V flop per step (2 fwd + 2 z-recompute + 2 dZ.W)",
+                     "peak_source": f"{peaks['source']} bf16_tflops_sustained"},
+        "components_ms": {"linear_logp_fwd": fwd_ms, "linear_logp_bwd": bwd_ms,
+                          "logits_path": lg_ms},
+        "fwd_tflops": flops_fwd / (fwd_ms / 1000.0) / 1e12,
+        "bwd_tflops": flops_bwd / (bwd_ms / 1000.0) / 1e12,
+        "logits_path": {"bound": "hbm", "achieved": lg_gbs, "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": lg_gbs / peaks["hbm_gbs"],
+                        "bytes_per_call": lg_bytes, "us_per_call": lg_ms * 1000.0,
+                        "tokens_per_s": Tl / (lg_ms / 1000.0)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+        "device": torch.cuda.get_device_name(dev),
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

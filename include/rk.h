@@ -1,0 +1,165 @@
+/*
+ * rk.h -- C ABI of the batch-invariant selected-token logprob library (librk).
+ *
+ * The operators are the selected-logprob members of the P0 kernel suite named
+ * in RL-Kernel issue #101 "[RFC] Batch-Invariant RL Kernel Suite for
+ * Train-Inference Consistency" (maintainer comment, P0 operator list:
+ * "lm_head, linear_logp, logp/batch_invariant_logp") and ordered in the
+ * forward chain of PR #264 "docs(ws1): batch-invariance contract RFC"
+ * (First-Divergence Localization: 6 lm_head, 7 linear_logp, 8 logp).
+ *
+ * Contract every entry point keeps (issue #101, maintainer comment, relation
+ * table; PR #264, relation I): for a given logical token row, the outputs are
+ * bitwise identical whatever the batch around it -- batch size (T1), the row's
+ * position (T2), the content of other rows (T3), padding (T4) and varlen
+ * packing or selection (T6).  The kernels use one tile shape and one
+ * reduction order per (H, V) for every T, and no atomics in any result.
+ *
+ * Conventions shared by all entry points
+ *  - All tensor pointers are DEVICE pointers, owned by the caller, contiguous
+ *    row-major.  The library never allocates device memory; scratch space is
+ *    passed in as `workspace`.  Outputs must not alias inputs or each other.
+ *  - bf16 tensors are passed as `const uint16_t*` (IEEE bfloat16 bit patterns).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *    asynchronous and stream-ordered; none synchronises the host.
+ *  - Active rows.  Row t is active iff targets[t] >= 0 and, when cu_seqlens is
+ *    not NULL, cu_seqlens[0] <= t < cu_seqlens[num_seqs].  Inactive rows get
+ *    logp = lse = 0 and dh = 0, and their inputs (even NaN) never reach an
+ *    active row.  (Issue #244 "[WS1 Test] #154 dtype pin + #152 KV path + #153
+ *    bwd invariance + #150 chain gate", Workstream 3, Logical-workload
+ *    identity: padding is excluded from outputs and gradients.)
+ *    cu_seqlens (int32, num_seqs + 1 ascending offsets) only bounds the active
+ *    range; the operators are per token.
+ *  - A target >= V on an active row is an input error found on the device:
+ *    that row's outputs become NaN and the device error word gets
+ *    RK_DEVERR_TARGET_RANGE (read it with rk_get_device_error).  Nothing traps.
+ *  - Precision (issue #244, Workstream 1 #154, Scope table: bf16 inputs,
+ *    fp32 accumulation): bf16 inputs, fp32 tensor-core accumulation, fp32
+ *    outputs.  Results match the fp64 definition within
+ *    |d logp| <= 1e-3 + 1e-3 |logp| and |d dh| <= 1e-3 + 1e-3 max|dh|.
+ *  - Argument errors return a status before anything is launched.  Launch
+ *    failures return RK_ERR_CUDA (the CUDA error is left for
+ *    cudaGetLastError / rk_last_cuda_error).
+ *  - Thread safety: entry points may be called from several host threads; the
+ *    only shared state is a per-device cache of function pointers.
+ */
+#ifndef RK_H
+#define RK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RK_OK = 0,
+    RK_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, bad cu_seqlens count, ... */
+    RK_ERR_UNSUPPORTED = 2,  /* shape outside the supported set (e.g. H % 64 != 0) */
+    RK_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than the *_workspace_size query */
+    RK_ERR_CUDA = 4          /* a CUDA runtime call or launch failed */
+} rk_status;
+
+/* Device error word bits (rk_get_device_error). */
+#define RK_DEVERR_TARGET_RANGE 0x1  /* an active row had target >= V */
+#define RK_DEVERR_TIMEOUT 0x2       /* a pipeline wait gave up after its time limit */
+
+/*
+ * Bytes of workspace rk_linear_logp needs for T rows (>= 0).  The layout is
+ * private: per-row, per-vocab-tile (max, sum-exp) partials plus the target
+ * logit of every row.  Returns 0 if T == 0.
+ */
+size_t rk_linear_logp_workspace_size(int64_t T, int64_t H, int64_t V);
+
+/*
+ * linear_logp forward: for every active row t,
+ *     z[t, v]  = sum_k h[t, k] * W[v, k]            (z = h . W^T, fp32 accumulation)
+ *     lse[t]   = log sum_v exp(z[t, v])
+ *     logp[t]  = z[t, targets[t]] - lse[t]
+ * without writing z to memory (issue #101, maintainer comment, P0 list
+ * "linear_logp"; PR #264 chain index 7).
+ *
+ *   h         bf16 [T, H]   hidden states, row-major, 16-byte aligned
+ *   W         bf16 [V, H]   lm_head weight (row v is the weight of token v), 16-byte aligned
+ *   targets   int64 [T]     selected token of each row (< 0: row inactive)
+ *   cu_seqlens int32 [num_seqs + 1] or NULL
+ *   logp      fp32 [T]      output
+ *   lse       fp32 [T]      output (log-sum-exp of each row), or NULL
+ *   workspace device scratch of >= rk_linear_logp_workspace_size(T, H, V) bytes,
+ *             256-byte aligned; contents on entry are ignored.
+ * Supported: H % 64 == 0, H <= 65536; 1 <= V < 2^31; 0 <= T < 2^31 (T == 0 is a no-op).
+ */
+rk_status rk_linear_logp(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                         const int32_t *cu_seqlens, int32_t num_seqs,
+                         int64_t T, int64_t H, int64_t V,
+                         float *logp, float *lse,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Logits path ("logp / batch_invariant_logp", issue #101 P0 list; PR #264 chain
+ * index 8): from materialised logits,
+ *     lse[t]  = log sum_v exp(logits[t, v]),   logp[t] = logits[t, targets[t]] - lse[t].
+ *
+ *   logits    bf16 [T, V], row stride V elements; any 2-byte alignment (the
+ *             reduction order depends on column indices only, never on the
+ *             address, so a row's result does not depend on where it sits)
+ *   targets, cu_seqlens, num_seqs, logp, lse: as for rk_linear_logp (lse may be NULL)
+ * Supported: 1 <= V < 2^31, 0 <= T.  Needs no workspace.
+ */
+rk_status rk_logp_from_logits(const uint16_t *logits, const int64_t *targets,
+                              const int32_t *cu_seqlens, int32_t num_seqs,
+                              int64_t T, int64_t V, float *logp, float *lse, void *stream);
+
+/*
+ * Bytes of workspace rk_linear_logp_bwd needs to process all T rows in one
+ * pass (one bf16 [T, V] buffer of g * softmax probabilities, rounded up).
+ * A smaller workspace (but at least rk_linear_logp_bwd_min_workspace_size)
+ * makes the call process the rows in chunks; the results do not change.
+ */
+size_t rk_linear_logp_bwd_workspace_size(int64_t T, int64_t H, int64_t V);
+size_t rk_linear_logp_bwd_min_workspace_size(int64_t H, int64_t V);
+
+/*
+ * linear_logp backward with respect to h (issue #244, Workstream 3 #153:
+ * fixed, batch-shape-independent reduction order, no atomicAdd):
+ *     p[t, v]  = exp(z[t, v] - lse[t])
+ *     dh[t, :] = g[t] * (W[targets[t], :] - sum_v p[t, v] * W[v, :])
+ * for every active row (dh = 0 on inactive rows).
+ *
+ *   h, W, targets, cu_seqlens, num_seqs: as for rk_linear_logp
+ *   lse        fp32 [T]  the lse output of rk_linear_logp on the same inputs
+ *   grad_logp  fp32 [T]  upstream gradient g of each row's logp
+ *   dh         fp32 [T, H] output
+ *   workspace  >= rk_linear_logp_bwd_min_workspace_size(H, V) bytes, 256-byte aligned
+ * The sum over v runs in one fixed ascending order for every row (no split of
+ * V across blocks, no atomics); the probabilities enter that sum rounded to
+ * bf16, the one-hot term is applied in fp32.
+ */
+rk_status rk_linear_logp_bwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                             const int32_t *cu_seqlens, int32_t num_seqs,
+                             int64_t T, int64_t H, int64_t V,
+                             const float *lse, const float *grad_logp, float *dh,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Reads and clears the device error word of the current device after
+ * synchronising `stream`.  *err receives an OR of RK_DEVERR_* bits (0 = none).
+ * For tests and debugging; it is the only call that synchronises.
+ */
+rk_status rk_get_device_error(void *stream, int32_t *err);
+
+/* Human-readable name of a status code (static string). */
+const char *rk_status_string(rk_status s);
+
+/* The CUDA error code behind the last RK_ERR_CUDA returned on this host thread. */
+int rk_last_cuda_error(void);
+
+/* Library version, e.g. "rk 0.1.0 sm_103a". */
+const char *rk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RK_H */

@@ -1,0 +1,222 @@
+"""Batch-invariant selected-token logprob on GB300 (sm_103a).
+
+Thin Python binding over the C-ABI library ``librk.so`` (see ``include/rk.h``).
+This module only marshals arguments -- device pointers, sizes and the current
+CUDA stream -- and allocates outputs and workspace with PyTorch; every step of
+the computation runs in the library's CUDA kernels.  There is no CPU path: if
+``librk.so`` is missing or no GPU is present the calls raise.
+
+Operators (RL-Kernel issue #101, maintainer comment, P0 operator list):
+
+* :func:`linear_logp`      -- ``logp[t] = z[t, target_t] - logsumexp_v z[t, v]``, ``z = h W^T``
+* :func:`logp_from_logits` -- the same from materialised bf16 logits
+* :func:`linear_logp_bwd`  -- ``dh[t] = g[t] (W[target_t] - softmax(z[t]) W)``
+
+Each is bitwise invariant for a given logical row under changes of batch
+size, row position, neighbour content, padding and varlen packing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "RkError", "library_path", "load_library",
+    "linear_logp", "linear_logp_workspace_size",
+    "logp_from_logits",
+    "linear_logp_bwd", "linear_logp_bwd_workspace_size", "linear_logp_bwd_min_workspace_size",
+    "get_device_error", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "librk.so")
+_lib = None
+
+RK_OK, RK_ERR_INVALID_ARG, RK_ERR_UNSUPPORTED, RK_ERR_WORKSPACE, RK_ERR_CUDA = range(5)
+DEVERR_TARGET_RANGE = 0x1
+DEVERR_TIMEOUT = 0x2
+
+
+class RkError(RuntimeError):
+    def __init__(self, what: str, status: int, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        name = _lib.rk_status_string(status).decode() if _lib is not None else str(status)
+        msg = f"{what} failed: {name}"
+        if status == RK_ERR_CUDA:
+            msg += f" (cudaError {cuda_error})"
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load librk.so (built by ``invariant_rl_logprob_gb300.build``); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"{_LIB_PATH} is missing: build it with `python -m invariant_rl_logprob_gb300.build` "
+            "(there is no CPU fallback)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    lib.rk_linear_logp_workspace_size.argtypes = [i64, i64, i64]
+    lib.rk_linear_logp_workspace_size.restype = sz
+    lib.rk_linear_logp.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, sz, vp]
+    lib.rk_linear_logp.restype = ctypes.c_int
+    lib.rk_logp_from_logits.argtypes = [vp, vp, vp, i32, i64, i64, vp, vp, vp]
+    lib.rk_logp_from_logits.restype = ctypes.c_int
+    lib.rk_linear_logp_bwd_workspace_size.argtypes = [i64, i64, i64]
+    lib.rk_linear_logp_bwd_workspace_size.restype = sz
+    lib.rk_linear_logp_bwd_min_workspace_size.argtypes = [i64, i64]
+    lib.rk_linear_logp_bwd_min_workspace_size.restype = sz
+    lib.rk_linear_logp_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, sz, vp]
+    lib.rk_linear_logp_bwd.restype = ctypes.c_int
+    lib.rk_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
+    lib.rk_get_device_error.restype = ctypes.c_int
+    lib.rk_status_string.argtypes = [ctypes.c_int]
+    lib.rk_status_string.restype = ctypes.c_char_p
+    lib.rk_last_cuda_error.argtypes = []
+    lib.rk_last_cuda_error.restype = ctypes.c_int
+    lib.rk_version.argtypes = []
+    lib.rk_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != RK_OK:
+        raise RkError(what, status, _lib.rk_last_cuda_error() if status == RK_ERR_CUDA else 0)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path), got {t.device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _rows(targets, cu_seqlens, T, device):
+    _need(targets, "targets", torch.int64, 1)
+    if targets.shape[0] != T or targets.device != device:
+        raise ValueError("targets must be [T] on the same device")
+    if cu_seqlens is None:
+        return None, 0
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if cu_seqlens.device != device or cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must be a non-empty int32 tensor on the same device")
+    return cu_seqlens, cu_seqlens.numel() - 1
+
+
+def linear_logp_workspace_size(T: int, H: int, V: int) -> int:
+    return int(load_library().rk_linear_logp_workspace_size(T, H, V))
+
+
+def linear_logp(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor,
+                cu_seqlens: torch.Tensor | None = None, *, out: torch.Tensor | None = None,
+                lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                stream: torch.cuda.Stream | None = None):
+    """Selected-token logprob of ``h W^T``: returns ``(logp, lse)``, fp32 ``[T]``."""
+    lib = load_library()
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    T, H = h.shape
+    V = W.shape[0]
+    if W.shape[1] != H or W.device != h.device:
+        raise ValueError("W must be [V, H] on h's device")
+    cu, ns = _rows(targets, cu_seqlens, T, h.device)
+    if out is None:
+        out = torch.empty(T, dtype=torch.float32, device=h.device)
+    if lse is None:
+        lse = torch.empty(T, dtype=torch.float32, device=h.device)
+    need = int(lib.rk_linear_logp_workspace_size(T, H, V))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
+    st = lib.rk_linear_logp(_ptr(h), _ptr(W), _ptr(targets), _ptr(cu), ns, T, H, V,
+                            _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                            _stream_handle(stream, h.device))
+    _check(st, "rk_linear_logp")
+    return out, lse
+
+
+def logp_from_logits(logits: torch.Tensor, targets: torch.Tensor,
+                     cu_seqlens: torch.Tensor | None = None, *, out: torch.Tensor | None = None,
+                     lse: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None):
+    """Selected-token logprob from bf16 logits ``[T, V]``: returns ``(logp, lse)``."""
+    lib = load_library()
+    _need(logits, "logits", torch.bfloat16, 2)
+    T, V = logits.shape
+    cu, ns = _rows(targets, cu_seqlens, T, logits.device)
+    if out is None:
+        out = torch.empty(T, dtype=torch.float32, device=logits.device)
+    if lse is None:
+        lse = torch.empty(T, dtype=torch.float32, device=logits.device)
+    st = lib.rk_logp_from_logits(_ptr(logits), _ptr(targets), _ptr(cu), ns, T, V, _ptr(out),
+                                 _ptr(lse), _stream_handle(stream, logits.device))
+    _check(st, "rk_logp_from_logits")
+    return out, lse
+
+
+def linear_logp_bwd_workspace_size(T: int, H: int, V: int) -> int:
+    return int(load_library().rk_linear_logp_bwd_workspace_size(T, H, V))
+
+
+def linear_logp_bwd_min_workspace_size(H: int, V: int) -> int:
+    return int(load_library().rk_linear_logp_bwd_min_workspace_size(H, V))
+
+
+def linear_logp_bwd(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
+                    grad_logp: torch.Tensor, cu_seqlens: torch.Tensor | None = None, *,
+                    dh: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                    stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """dh = g (W[target] - softmax(h W^T) W) in fp32 ``[T, H]``."""
+    lib = load_library()
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    T, H = h.shape
+    V = W.shape[0]
+    if W.shape[1] != H or W.device != h.device:
+        raise ValueError("W must be [V, H] on h's device")
+    cu, ns = _rows(targets, cu_seqlens, T, h.device)
+    _need(lse, "lse", torch.float32, 1)
+    _need(grad_logp, "grad_logp", torch.float32, 1)
+    if dh is None:
+        dh = torch.empty((T, H), dtype=torch.float32, device=h.device)
+    if workspace is None:
+        need = int(lib.rk_linear_logp_bwd_workspace_size(T, H, V))
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
+    st = lib.rk_linear_logp_bwd(_ptr(h), _ptr(W), _ptr(targets), _ptr(cu), ns, T, H, V,
+                                _ptr(lse), _ptr(grad_logp), _ptr(dh), _ptr(workspace),
+                                workspace.numel(), _stream_handle(stream, h.device))
+    _check(st, "rk_linear_logp_bwd")
+    return dh
+
+
+def get_device_error(stream: torch.cuda.Stream | None = None) -> int:
+    """Read and clear the device error word (synchronises the stream)."""
+    lib = load_library()
+    v = ctypes.c_int32(0)
+    _check(lib.rk_get_device_error(_stream_handle(stream, None), ctypes.byref(v)),
+           "rk_get_device_error")
+    return int(v.value)

@@ -1,0 +1,644 @@
+// linear_logp_tc.cu -- tensor-core kernels of linear_logp: the fused forward
+// and the two GEMMs of the backward.
+//
+// Forward ("linear_logp", RL-Kernel issue #101, maintainer comment, P0
+// operator list; chain index 7 of PR #264 "docs(ws1): batch-invariance
+// contract RFC"):
+//   z[t, v] = sum_k h[t, k] W[v, k],  lse[t] = log sum_v exp z[t, v],
+//   logp[t] = z[t, target_t] - lse[t];   z never leaves the chip.
+// Backward with respect to h (issue #244 "[WS1 Test] ...", Workstream 3 #153:
+// fixed, batch-shape-independent reduction order, no atomicAdd):
+//   dZ[t, v] = g[t] exp(z[t, v] - lse[t])                     (GEMM 1, stored bf16)
+//   dh[t, :] = g[t] W[target_t, :] - sum_v dZ[t, v] W[v, :]    (GEMM 2, fp32)
+//
+// One persistent, warp-specialised tile kernel serves the three GEMMs:
+//   warp 4      TMA producer: 128x64 tiles of A and 256x64 (K-major) or 64x256
+//               (MN-major) tiles of B through a 4-stage shared-memory ring,
+//               128-byte swizzle;
+//   warp 5      allocates 512 TMEM columns and issues tcgen05.mma (M=128,
+//               N=256, K=16, bf16 x bf16 -> fp32) into one of two 256-column
+//               accumulators;
+//   warps 0-3   epilogue: thread i owns tile row i (TMEM lane i) and drains the
+//               other accumulator while the next tile accumulates.
+// Epilogues:
+//   kFwd  the row's softmax partial over the tile's 256 vocabulary columns,
+//         m = max z, s = sum 2^((z - m) log2 e), and z[target] if the target
+//         is in the tile, written to workspace[row][tile];
+//   kDz   dZ = g exp(z - lse) rounded to bf16 (0 on inactive rows);
+//   kDh   dh = g W[target] - acc in fp32 (0 on inactive rows).
+// A second small kernel (linear_logp_merge) folds the forward partials of a
+// row in a fixed order into lse and logp.
+//
+// Batch invariance by construction: the tile shape, the K order (64-wide
+// stages ascending, 16-wide MMAs ascending inside a stage), the epilogue's
+// column order and the merge order are identical for every T; a row's results
+// depend only on that row's inputs and on W (rows of a tensor-core tile do not
+// interact), never on the tile, CTA or M position that holds the row, on the
+// schedule, or on how the backward cuts T into chunks.  V is never split
+// across CTAs in the backward's sum (no split-K) and no atomics touch results.
+#include <algorithm>
+
+#include "rk_device.cuh"
+#include "rk_internal.h"
+
+namespace rk {
+namespace {
+
+constexpr int BM = 128;  // tile rows (TMEM lanes)
+constexpr int BN = 256;  // tile columns (TMEM columns per accumulator)
+constexpr int BK = 64;   // K per pipeline stage (64 bf16 = one 128-byte swizzle row)
+constexpr int UK = 16;   // K per tcgen05.mma of kind::f16
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;
+constexpr int kBBytes = BN * BK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kEpiThreads = 128;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = kEpiThreads + 64;
+constexpr int kGroupN = 16;  // raster group (in N tiles) of the forward / dZ GEMMs
+
+enum Mode { kFwd = 0, kDz = 1, kDh = 2 };
+
+struct Ctl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(Ctl);
+
+struct TileArgs {
+    // row masking (global row index t = row0 + local row)
+    const int64_t *targets;
+    const int32_t *cu;
+    int32_t num_seqs;
+    int64_t row0;
+    int64_t rows;  // rows of this launch (local)
+    int32_t V;
+    int32_t num_m, num_n, num_k;
+    unsigned *err;
+    // kFwd
+    float2 *part;  // [rows][num_n]
+    float *ztgt;   // [rows]
+    // kDz
+    const float *lse;   // [T] (global)
+    const float *grad;  // [T] (global)
+    uint16_t *dz;       // [rows][ldz] bf16
+    int64_t ldz;
+    // kDh
+    const uint16_t *W;  // [V][H]
+    float *dh;          // [T][H] (global)
+    int32_t H;
+};
+
+// Every lane waits; the warp proceeds only if all lanes saw the phase complete,
+// so the warp-collective TMEM loads that follow are never reached divergently.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          unsigned *err) {
+    const bool ok = mbar_wait(bar, parity, abort, err);
+    return __all_sync(0xffffffffu, ok) != 0;
+}
+
+template <int MODE>
+__device__ __forceinline__ void tile_coords(int64_t tile, const TileArgs &a, int &mb, int &nb) {
+    if constexpr (MODE == kDh) {
+        // every H tile of a row block before the next row block: CTAs running
+        // together share A (dZ rows) and walk W's K (vocabulary) rows in step
+        mb = (int)(tile / a.num_n);
+        nb = (int)(tile - (int64_t)mb * a.num_n);
+    } else {
+        const int64_t per_group = (int64_t)a.num_m * kGroupN;
+        const int64_t g = tile / per_group;
+        const int64_t r = tile - g * per_group;
+        const int n0 = (int)g * kGroupN;
+        const int gn = min(kGroupN, a.num_n - n0);
+        mb = (int)(r / gn);
+        nb = n0 + (int)(r % gn);
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_logp_tiles(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const TileArgs a) {
+    // kDh: B is W read as [K = vocabulary rows, N = H columns] (N contiguous,
+    // "MN-major"), staged as four 64-column boxes of BK rows each.
+    constexpr bool kBmn = (MODE == kDh);
+    constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, false, kBmn);
+    constexpr uint32_t kBBoxBytes = BK * 64 * 2;  // one 64-column MN-major box
+    // Descriptor strides.  K-major, 128B swizzle: 8-row groups 1024 B apart;
+    // the next 16-wide K slice starts 32 B further.  MN-major, 128B swizzle:
+    // 64-column atoms kBBoxBytes apart (leading offset), 8-row K groups 1024 B
+    // apart (stride offset); the next 16-row K slice starts 16*128 B further.
+    constexpr uint32_t kBLbo = kBmn ? kBBoxBytes : 16;
+    constexpr uint32_t kBStepK = kBmn ? (UK * 128) : (UK * 2);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)kStages * kStageBytes);
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t total = (int64_t)a.num_m * a.num_n;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&ctl->tmem_full[b]), 1);
+            mbar_init(smem_u32(&ctl->tmem_empty[b]), kEpiThreads);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    volatile int *abort = &ctl->abort;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t last_ph[kStages];
+            bool used[kStages];
+            for (int i = 0; i < kStages; ++i) {
+                used[i] = false;
+                last_ph[i] = 0;
+            }
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords<MODE>(tile, a, mb, nb);
+                for (int kb = 0; kb < a.num_k; ++kb) {
+                    if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&ctl->full[s]);
+                    const uint32_t sa = sbase + (uint32_t)(s * kStageBytes);
+                    if constexpr (kBmn) {
+                        // only the 64-column boxes that start inside H are loaded; the
+                        // accumulator columns of the others are never stored
+                        const int nbox = min(BN / 64, (a.H - nb * BN) / 64);
+                        mbar_arrive_expect_tx(fb, (uint32_t)(kABytes + nbox * (int)kBBoxBytes));
+                        tma_load_2d(sa, &tmA, fb, kb * BK, mb * BM);
+                        for (int j = 0; j < nbox; ++j)
+                            tma_load_2d(sa + kABytes + j * kBBoxBytes, &tmB, fb, nb * BN + j * 64,
+                                        kb * BK);
+                    } else {
+                        mbar_arrive_expect_tx(fb, kStageBytes);
+                        tma_load_2d(sa, &tmA, fb, kb * BK, mb * BM);
+                        tma_load_2d(sa + kABytes, &tmB, fb, kb * BK, nb * BN);
+                    }
+                    used[s] = true;
+                    last_ph[s] = ph;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {  // let every issued copy land before the block exits
+                for (int i = 0; i < kStages; ++i)
+                    if (used[i]) mbar_wait_drain(smem_u32(&ctl->full[i]), last_ph[i], 100000000ull);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int b = 0;
+            uint32_t tph = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                if (!mbar_wait(smem_u32(&ctl->tmem_empty[b]), tph ^ 1u, abort, a.err)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(b * BN);
+                for (int kb = 0; kb < a.num_k; ++kb) {
+                    if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + (uint32_t)(s * kStageBytes);
+                    const uint64_t ad = smem_desc_sw128(sa, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(sa + kABytes, kBLbo, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UK; ++kk) {
+                        mma_bf16_ss(d, ad + (uint64_t)((kk * UK * 2) >> 4),
+                                    bd + (uint64_t)((kk * kBStepK) >> 4), kIdesc,
+                                    (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&ctl->empty[s]));
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&ctl->tmem_full[b]));
+                if (++b == 2) {
+                    b = 0;
+                    tph ^= 1u;
+                }
+            }
+            // No MMA may still be writing TMEM when the block releases it.
+            mma_commit(smem_u32(&ctl->drain));
+            mbar_wait_drain(smem_u32(&ctl->drain), 0, 1000000000ull);
+        }
+    } else {
+        // Epilogue: warp w reads TMEM lanes [32w, 32w+32) = tile rows.
+        int b = 0;
+        uint32_t tph = 0;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords<MODE>(tile, a, mb, nb);
+            const int64_t lrow = (int64_t)mb * BM + threadIdx.x;  // local row
+            const bool in_range = lrow < a.rows;
+            const int64_t grow = a.row0 + lrow;                    // global row
+            const int64_t tgt = in_range ? a.targets[grow] : -1;
+            const int n0 = nb * BN;
+
+            if constexpr (MODE == kFwd) {
+                const int valid = min(BN, a.V - n0);
+                const int tcol = (tgt >= n0 && tgt < (int64_t)n0 + valid) ? (int)(tgt - n0) : -1;
+                if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
+                tc_fence_after();
+                const uint32_t taddr = tmem + lane_off + (uint32_t)(b * BN);
+                // pass 1: the row's maximum over the tile
+                float m = -INFINITY;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
+                    tmem_ld_wait();
+                    if (valid == BN) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) m = fmaxf(m, __uint_as_float(r[j]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (c * 32 + j < valid) m = fmaxf(m, __uint_as_float(r[j]));
+                    }
+                }
+                // pass 2: sum of 2^((z - m) log2 e), four accumulators in a fixed pattern
+                const float mb2 = __fmul_rn(-m, kLog2e);
+                float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+                float zt = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
+                    tmem_ld_wait();
+                    float e[32];
+                    if (valid == BN) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            e[j] = ex2(__fmaf_rn(__uint_as_float(r[j]), kLog2e, mb2));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            e[j] = (c * 32 + j < valid)
+                                       ? ex2(__fmaf_rn(__uint_as_float(r[j]), kLog2e, mb2))
+                                       : 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        acc0 = __fadd_rn(acc0, e[j]);
+                        acc1 = __fadd_rn(acc1, e[j + 1]);
+                        acc2 = __fadd_rn(acc2, e[j + 2]);
+                        acc3 = __fadd_rn(acc3, e[j + 3]);
+                    }
+                    const int rel = tcol - c * 32;
+                    if (rel >= 0 && rel < 32) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j == rel) zt = __uint_as_float(r[j]);
+                    }
+                }
+                const float s = __fadd_rn(__fadd_rn(acc0, acc1), __fadd_rn(acc2, acc3));
+                tc_fence_before();
+                mbar_arrive(smem_u32(&ctl->tmem_empty[b]));
+                if (in_range) {
+                    a.part[lrow * a.num_n + nb] = make_float2(m, s);
+                    if (tcol >= 0) a.ztgt[lrow] = zt;
+                }
+            } else if constexpr (MODE == kDz) {
+                const bool active = in_range && row_active(grow, tgt, a.cu, a.num_seqs);
+                const float g = active ? a.grad[grow] : 0.f;
+                const float nl = active ? __fmul_rn(-a.lse[grow], kLog2e) : 0.f;
+                const int valid = min(BN, a.V - n0);
+                if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
+                tc_fence_after();
+                const uint32_t taddr = tmem + lane_off + (uint32_t)(b * BN);
+                uint16_t *drow = a.dz + lrow * a.ldz + n0;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float p0 = ex2(__fmaf_rn(__uint_as_float(r[2 * j]), kLog2e, nl));
+                        const float p1 = ex2(__fmaf_rn(__uint_as_float(r[2 * j + 1]), kLog2e, nl));
+                        const float d0 = active ? __fmul_rn(g, p0) : 0.f;
+                        const float d1 = active ? __fmul_rn(g, p1) : 0.f;
+                        pk[j] = pack_bf16x2(d0, d1);
+                    }
+                    if (in_range) {
+                        const int c0 = c * 32;
+                        if (c0 + 32 <= valid) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(drow + c0);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (c0 + j < valid)
+                                    drow[c0 + j] = (uint16_t)((j & 1) ? (pk[j >> 1] >> 16) : (pk[j >> 1] & 0xFFFFu));
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&ctl->tmem_empty[b]));
+            } else {  // kDh
+                const bool active = in_range && row_active(grow, tgt, a.cu, a.num_seqs) && tgt < a.V;
+                const float g = active ? a.grad[grow] : 0.f;
+                const uint16_t *wrow = a.W + (active ? tgt : 0) * (int64_t)a.H + n0;
+                const int hvalid = min(BN, a.H - n0);  // a multiple of 64
+                if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
+                tc_fence_after();
+                const uint32_t taddr = tmem + lane_off + (uint32_t)(b * BN);
+                float *orow = a.dh + grow * (int64_t)a.H + n0;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
+                    tmem_ld_wait();
+                    if (in_range && c * 32 < hvalid) {
+                        float o[32];
+                        if (active) {
+                            uint4 wv[4];
+                            const uint4 *src = reinterpret_cast<const uint4 *>(wrow + c * 32);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) wv[q] = __ldg(src + q);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const uint32_t w4[4] = {wv[q].x, wv[q].y, wv[q].z, wv[q].w};
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const int j = q * 8 + u * 2;
+                                    o[j] = __fmaf_rn(g, bf16_lo(w4[u]), -__uint_as_float(r[j]));
+                                    o[j + 1] = __fmaf_rn(g, bf16_hi(w4[u]), -__uint_as_float(r[j + 1]));
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) o[j] = 0.f;
+                        }
+                        float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&ctl->tmem_empty[b]));
+            }
+            if (++b == 2) {
+                b = 0;
+                tph ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+constexpr int kMergeRowsPerBlock = 8;
+
+__global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
+    linear_logp_merge(const float2 *__restrict__ part, const float *__restrict__ ztgt,
+                      const int64_t *__restrict__ targets, const int32_t *__restrict__ cu,
+                      int num_seqs, int64_t T, int32_t V, int32_t num_n, float *__restrict__ logp,
+                      float *__restrict__ lse, unsigned *err) {
+    const int64_t row = (int64_t)blockIdx.x * kMergeRowsPerBlock + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= T) return;
+    const int64_t tgt = targets[row];
+    if (!row_active(row, tgt, cu, num_seqs)) {
+        if (lane == 0) {
+            logp[row] = 0.f;
+            if (lse) lse[row] = 0.f;
+        }
+        return;
+    }
+    if (tgt >= V) {
+        if (lane == 0) {
+            logp[row] = __int_as_float(0x7fc00000);
+            if (lse) lse[row] = __int_as_float(0x7fc00000);
+            atomicOr(err, kErrTargetRange);
+        }
+        return;
+    }
+    const float2 *pr = part + row * num_n;
+    float m = -INFINITY, s = 0.f;
+#pragma unroll 4
+    for (int j = lane; j < num_n; j += 32) {
+        const float2 p = pr[j];
+        lse_merge(m, s, p.x, p.y);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+        const float so = __shfl_xor_sync(0xffffffffu, s, off);
+        lse_merge(m, s, mo, so);
+    }
+    if (lane == 0) {
+        const float l = __fadd_rn(m, logf(s));
+        logp[row] = __fsub_rn(ztgt[row], l);
+        if (lse) lse[row] = l;
+    }
+}
+
+// Backward rows with a target >= V get NaN gradients (and the error bit).
+__global__ void linear_logp_bwd_badtarget(const int64_t *__restrict__ targets,
+                                          const int32_t *__restrict__ cu, int num_seqs, int64_t T,
+                                          int32_t V, int32_t H, float *__restrict__ dh,
+                                          unsigned *err) {
+    const int64_t row = blockIdx.x;
+    if (row >= T) return;
+    const int64_t tgt = targets[row];
+    if (!row_active(row, tgt, cu, num_seqs) || tgt < V) return;
+    for (int k = threadIdx.x; k < H; k += blockDim.x) dh[row * H + k] = __int_as_float(0x7fc00000);
+    if (threadIdx.x == 0) atomicOr(err, kErrTargetRange);
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+template <int MODE>
+cudaError_t set_smem_attr(const DeviceInfo &di) {
+    static thread_local int done_dev = -1;
+    if (done_dev == di.device) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(linear_logp_tiles<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e == cudaSuccess) done_dev = di.device;
+    return e;
+}
+
+template <int MODE>
+cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const TileArgs &a,
+                      const DeviceInfo &di, cudaStream_t st) {
+    cudaError_t e = set_smem_attr<MODE>(di);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (int64_t)a.num_m * a.num_n;
+    if (tiles == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)std::min<int64_t>(tiles, di.sm_count);
+    linear_logp_tiles<MODE><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, a);
+    return cudaGetLastError();
+}
+
+int64_t ld_dz(int64_t V) { return (V + 7) / 8 * 8; }  // 16-byte aligned dZ rows
+
+}  // namespace
+
+size_t linear_fwd_workspace_bytes(int64_t T, int64_t V) {
+    if (T <= 0) return 0;
+    const int64_t num_n = (V + BN - 1) / BN;
+    return round256((size_t)T * (size_t)num_n * sizeof(float2)) + round256((size_t)T * sizeof(float));
+}
+
+cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                              const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
+                              float *logp, float *lse, void *workspace, const DeviceInfo &di,
+                              cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    CUtensorMap tmA, tmB;
+    if (!encode_tmap_bf16_2d(&tmA, h, (uint64_t)H, (uint64_t)T, (uint64_t)H * 2, BK, BM, true))
+        return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16_2d(&tmB, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN, true))
+        return cudaErrorInvalidValue;
+
+    TileArgs a{};
+    a.targets = targets;
+    a.cu = cu;
+    a.num_seqs = num_seqs;
+    a.row0 = 0;
+    a.rows = T;
+    a.V = (int32_t)V;
+    a.H = (int32_t)H;
+    a.num_m = (int32_t)((T + BM - 1) / BM);
+    a.num_n = (int32_t)((V + BN - 1) / BN);
+    a.num_k = (int32_t)(H / BK);
+    a.err = di.err;
+    a.part = reinterpret_cast<float2 *>(workspace);
+    a.ztgt = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) +
+                                       round256((size_t)T * (size_t)a.num_n * sizeof(float2)));
+    cudaError_t e = run_tiles<kFwd>(tmA, tmB, a, di, st);
+    if (e != cudaSuccess) return e;
+
+    const unsigned mgrid = (unsigned)((T + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock);
+    linear_logp_merge<<<mgrid, 32 * kMergeRowsPerBlock, 0, st>>>(a.part, a.ztgt, targets, cu,
+                                                                  num_seqs, T, a.V, a.num_n, logp,
+                                                                  lse, di.err);
+    return cudaGetLastError();
+}
+
+int64_t linear_bwd_chunk_quantum() { return BM; }
+
+size_t linear_bwd_chunk_bytes(int64_t rows, int64_t V) {
+    return round256((size_t)rows * (size_t)ld_dz(V) * 2);
+}
+
+cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                              const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
+                              const float *lse, const float *grad, float *dh, void *workspace,
+                              size_t workspace_bytes, const DeviceInfo &di, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const int64_t ldz = ld_dz(V);
+    // rows per chunk: as many whole 128-row blocks as the workspace holds
+    int64_t chunk = (int64_t)(workspace_bytes / ((size_t)ldz * 2)) / BM * BM;
+    if (chunk <= 0) return cudaErrorInvalidValue;
+    if (chunk > T) chunk = T;
+    uint16_t *dz = reinterpret_cast<uint16_t *>(workspace);
+
+    CUtensorMap tmW_k, tmW_mn;
+    if (!encode_tmap_bf16_2d(&tmW_k, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN, true))
+        return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16_2d(&tmW_mn, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, 64, BK, true))
+        return cudaErrorInvalidValue;
+
+    for (int64_t r0 = 0; r0 < T; r0 += chunk) {
+        const int64_t rows = std::min(chunk, T - r0);
+        CUtensorMap tmH, tmDz;
+        if (!encode_tmap_bf16_2d(&tmH, h + r0 * H, (uint64_t)H, (uint64_t)rows, (uint64_t)H * 2, BK,
+                                 BM, true))
+            return cudaErrorInvalidValue;
+        if (!encode_tmap_bf16_2d(&tmDz, dz, (uint64_t)V, (uint64_t)rows, (uint64_t)ldz * 2, BK, BM,
+                                 true))
+            return cudaErrorInvalidValue;
+
+        TileArgs a{};
+        a.targets = targets;
+        a.cu = cu;
+        a.num_seqs = num_seqs;
+        a.row0 = r0;
+        a.rows = rows;
+        a.V = (int32_t)V;
+        a.H = (int32_t)H;
+        a.err = di.err;
+        a.lse = lse;
+        a.grad = grad;
+        a.dz = dz;
+        a.ldz = ldz;
+        a.W = W;
+        a.dh = dh;
+        a.num_m = (int32_t)((rows + BM - 1) / BM);
+
+        // GEMM 1: z recomputed, dZ = g exp(z - lse) in bf16
+        a.num_n = (int32_t)((V + BN - 1) / BN);
+        a.num_k = (int32_t)(H / BK);
+        cudaError_t e = run_tiles<kDz>(tmH, tmW_k, a, di, st);
+        if (e != cudaSuccess) return e;
+
+        // GEMM 2: dh = g W[target] - dZ W, K = V in one ascending pass
+        a.num_n = (int32_t)((H + BN - 1) / BN);
+        a.num_k = (int32_t)((V + BK - 1) / BK);
+        e = run_tiles<kDh>(tmDz, tmW_mn, a, di, st);
+        if (e != cudaSuccess) return e;
+    }
+    linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(targets, cu, num_seqs, T, (int32_t)V,
+                                                          (int32_t)H, dh, di.err);
+    return cudaGetLastError();
+}
+
+}  // namespace rk

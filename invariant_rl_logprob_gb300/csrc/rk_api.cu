@@ -1,0 +1,239 @@
+// rk_api.cu -- the extern "C" entry points declared in include/rk.h:
+// argument validation (before any launch), per-device lookups, TMA descriptor
+// encoding, and dispatch to the kernels' launchers.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "../../include/rk.h"
+#include "rk_internal.h"
+
+// One error word per device (the module is loaded per device context).
+__device__ unsigned int g_rk_device_error = 0u;
+
+namespace rk {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices] = {};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+thread_local int g_last_cuda_error = 0;
+
+void load_encode() {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, uint32_t esize, const void *base,
+               uint64_t inner, uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+               uint32_t box_outer, bool sw128) {
+    std::call_once(g_encode_once, load_encode);
+    if (!g_encode) return false;
+    (void)esize;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+rk_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return RK_ERR_CUDA;
+}
+
+}  // namespace
+
+bool encode_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                         bool sw128) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, outer,
+                     row_stride_bytes, box_inner, box_outer, sw128);
+}
+
+bool encode_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                        bool sw128) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, inner, outer,
+                     row_stride_bytes, box_inner, box_outer, sw128);
+}
+
+cudaError_t current_device_info(DeviceInfo *di) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_dev_ready[dev]) {
+            *di = g_dev[dev];
+            return cudaSuccess;
+        }
+    }
+    DeviceInfo d;
+    d.device = dev;
+    e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_rk_device_error);
+    if (e != cudaSuccess) return e;
+    d.err = static_cast<unsigned *>(p);
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_dev[dev] = d;
+    g_dev_ready[dev] = true;
+    *di = d;
+    return cudaSuccess;
+}
+
+}  // namespace rk
+
+using rk::DeviceInfo;
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+rk_status check_rows(const int64_t *targets, const int32_t *cu, int32_t num_seqs) {
+    if (!targets) return RK_ERR_INVALID_ARG;
+    if (cu && num_seqs < 0) return RK_ERR_INVALID_ARG;
+    return RK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *rk_status_string(rk_status s) {
+    switch (s) {
+        case RK_OK: return "RK_OK";
+        case RK_ERR_INVALID_ARG: return "RK_ERR_INVALID_ARG";
+        case RK_ERR_UNSUPPORTED: return "RK_ERR_UNSUPPORTED";
+        case RK_ERR_WORKSPACE: return "RK_ERR_WORKSPACE";
+        case RK_ERR_CUDA: return "RK_ERR_CUDA";
+    }
+    return "RK_ERR_UNKNOWN";
+}
+
+int rk_last_cuda_error(void) { return rk::g_last_cuda_error; }
+
+const char *rk_version(void) { return "rk 0.1.0 sm_103a"; }
+
+size_t rk_linear_logp_workspace_size(int64_t T, int64_t H, int64_t V) {
+    (void)H;
+    if (T <= 0 || V <= 0) return 0;
+    return rk::linear_fwd_workspace_bytes(T, V);
+}
+
+rk_status rk_linear_logp(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                         const int32_t *cu_seqlens, int32_t num_seqs, int64_t T, int64_t H,
+                         int64_t V, float *logp, float *lse, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+    if (T < 0 || H <= 0 || V <= 0) return RK_ERR_INVALID_ARG;
+    if (T == 0) return RK_OK;
+    if (!h || !W || !logp) return RK_ERR_INVALID_ARG;
+    rk_status st = check_rows(targets, cu_seqlens, num_seqs);
+    if (st != RK_OK) return st;
+    if (H % 64 != 0 || H > 65536 || V >= (int64_t(1) << 31) || T >= (int64_t(1) << 31))
+        return RK_ERR_UNSUPPORTED;
+    if (!aligned(h, 16) || !aligned(W, 16)) return RK_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < rk::linear_fwd_workspace_bytes(T, V))
+        return RK_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return RK_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    e = rk::launch_linear_fwd(h, W, targets, cu_seqlens, num_seqs, T, H, V, logp, lse, workspace,
+                              di, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    return RK_OK;
+}
+
+rk_status rk_logp_from_logits(const uint16_t *logits, const int64_t *targets,
+                              const int32_t *cu_seqlens, int32_t num_seqs, int64_t T, int64_t V,
+                              float *logp, float *lse, void *stream) {
+    if (T < 0 || V <= 0) return RK_ERR_INVALID_ARG;
+    if (T == 0) return RK_OK;
+    if (!logits || !logp) return RK_ERR_INVALID_ARG;
+    rk_status st = check_rows(targets, cu_seqlens, num_seqs);
+    if (st != RK_OK) return st;
+    if (V >= (int64_t(1) << 31)) return RK_ERR_UNSUPPORTED;
+    if (!aligned(logits, 2)) return RK_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    e = rk::launch_logits_logp(logits, targets, cu_seqlens, num_seqs, T, V, logp, lse, di,
+                               static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    return RK_OK;
+}
+
+size_t rk_linear_logp_bwd_workspace_size(int64_t T, int64_t H, int64_t V) {
+    (void)H;
+    if (T <= 0 || V <= 0) return 0;
+    const int64_t q = rk::linear_bwd_chunk_quantum();
+    return rk::linear_bwd_chunk_bytes((T + q - 1) / q * q, V);
+}
+
+size_t rk_linear_logp_bwd_min_workspace_size(int64_t H, int64_t V) {
+    (void)H;
+    if (V <= 0) return 0;
+    return rk::linear_bwd_chunk_bytes(rk::linear_bwd_chunk_quantum(), V);
+}
+
+rk_status rk_linear_logp_bwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                             const int32_t *cu_seqlens, int32_t num_seqs, int64_t T, int64_t H,
+                             int64_t V, const float *lse, const float *grad_logp, float *dh,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+    if (T < 0 || H <= 0 || V <= 0) return RK_ERR_INVALID_ARG;
+    if (T == 0) return RK_OK;
+    if (!h || !W || !lse || !grad_logp || !dh) return RK_ERR_INVALID_ARG;
+    rk_status st = check_rows(targets, cu_seqlens, num_seqs);
+    if (st != RK_OK) return st;
+    if (H % 64 != 0 || H > 65536 || V >= (int64_t(1) << 31) || T >= (int64_t(1) << 31))
+        return RK_ERR_UNSUPPORTED;
+    if (!aligned(h, 16) || !aligned(W, 16) || !aligned(dh, 16)) return RK_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < rk_linear_logp_bwd_min_workspace_size(H, V))
+        return RK_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return RK_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    e = rk::launch_linear_bwd(h, W, targets, cu_seqlens, num_seqs, T, H, V, lse, grad_logp, dh,
+                              workspace, workspace_bytes, di, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    return RK_OK;
+}
+
+rk_status rk_get_device_error(void *stream, int32_t *err) {
+    if (!err) return RK_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned v = 0;
+    e = cudaMemcpyAsync(&v, di.err, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    e = cudaMemsetAsync(di.err, 0, sizeof(unsigned), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    *err = (int32_t)v;
+    return RK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,52 @@
+// rk_internal.h -- host-side declarations shared by the librk translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace rk {
+
+// Per-device facts the launchers need (cached by rk_api.cu).
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    unsigned *err = nullptr;  // device address of this device's error word
+};
+
+// Fills `di` for the current device (first call per device does the lookups).
+cudaError_t current_device_info(DeviceInfo *di);
+
+// Encodes a 2-D bf16 TMA descriptor over a row-major [outer, inner] matrix
+// with the given row stride (bytes) and box; 128-byte swizzle when `sw128`.
+// Returns false if the driver rejects it.
+bool encode_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                         bool sw128);
+// fp32 variant (used for TMA stores of fp32 tiles).
+bool encode_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                        bool sw128);
+
+// ---- logits path (logits_logp.cu) ----
+cudaError_t launch_logits_logp(const uint16_t *logits, const int64_t *targets, const int32_t *cu,
+                               int num_seqs, int64_t T, int64_t V, float *logp, float *lse,
+                               const DeviceInfo &di, cudaStream_t st);
+
+// ---- linear_logp forward (linear_logp_fwd.cu) ----
+size_t linear_fwd_workspace_bytes(int64_t T, int64_t V);
+cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                              const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
+                              float *logp, float *lse, void *workspace, const DeviceInfo &di,
+                              cudaStream_t st);
+
+// ---- linear_logp backward (linear_logp_bwd.cu) ----
+size_t linear_bwd_chunk_bytes(int64_t rows, int64_t V);
+int64_t linear_bwd_chunk_quantum();
+cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                              const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
+                              const float *lse, const float *grad, float *dh, void *workspace,
+                              size_t workspace_bytes, const DeviceInfo &di, cudaStream_t st);
+
+}  // namespace rk
