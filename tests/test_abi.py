@@ -1,0 +1,75 @@
+"""The C-ABI library builds, loads and exports every symbol include/rk.h
+declares (no compute calls: this runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            with open(os.path.join(ROOT, "include", fn)) as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(rk_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from invariant_rl_logprob_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_operators():
+    names = declared_symbols()
+    for n in ("rk_linear_logp", "rk_logp_from_logits", "rk_linear_logp_bwd",
+              "rk_linear_logp_workspace_size", "rk_linear_logp_bwd_workspace_size",
+              "rk_get_device_error", "rk_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_only_calls(lib):
+    lib.rk_status_string.restype = ctypes.c_char_p
+    lib.rk_status_string.argtypes = [ctypes.c_int]
+    assert lib.rk_status_string(0) == b"RK_OK"
+    assert lib.rk_status_string(3) == b"RK_ERR_WORKSPACE"
+    lib.rk_version.restype = ctypes.c_char_p
+    assert b"sm_103a" in lib.rk_version()
+    f = lib.rk_linear_logp_workspace_size
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int64] * 3
+    # T rows x ceil(V/256) tiles x 8 bytes + T x 4 bytes, each rounded to 256
+    assert f(8192, 4096, 128256) == 8192 * 501 * 8 + 8192 * 4
+    assert f(0, 4096, 128256) == 0
+    g = lib.rk_linear_logp_bwd_workspace_size
+    g.restype = ctypes.c_size_t
+    g.argtypes = [ctypes.c_int64] * 3
+    assert g(100, 64, 1001) == 128 * 1008 * 2
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    # invalid sizes are rejected on the host, without touching a device
+    f = lib.rk_linear_logp
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int32] + [ctypes.c_int64] * 3 + \
+        [ctypes.c_void_p] * 3 + [ctypes.c_size_t, ctypes.c_void_p]
+    assert f(None, None, None, None, 0, -1, 64, 10, None, None, None, 0, None) == 1
+    assert f(None, None, None, None, 0, 0, 64, 10, None, None, None, 0, None) == 0   # T = 0
+    assert f(None, None, None, None, 0, 4, 64, 10, None, None, None, 0, None) == 1   # NULL h
+    g = lib.rk_logp_from_logits
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int32] + [ctypes.c_int64] * 2 + \
+        [ctypes.c_void_p] * 3
+    assert g(None, None, None, 0, 5, 0, None, None, None) == 1                         # V = 0
