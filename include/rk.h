@@ -143,6 +143,35 @@ rk_status rk_linear_logp_bwd(const uint16_t *h, const uint16_t *W, const int64_t
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * rk_linear_logp without a workspace argument, for callers that cannot
+ * allocate device memory.  (No counterpart in the pages: this is an interface
+ * convenience, not part of the method.)  Such callers include programs whose
+ * device memory belongs to a fixed-budget arena or pool, where an extra
+ * cudaMalloc would fail against the budget, fragment the pool or stall the
+ * device (cudaMalloc and cudaFree may synchronise), and plugin-style hosts
+ * that hand over only input/output pointers and a stream.
+ *
+ * Same arguments, results and errors as rk_linear_logp, minus the workspace:
+ * the scratch lives in a fixed 32 MiB array inside the library (static device
+ * memory; every GPU on which the library is used keeps it until the process
+ * exits).  The call allocates nothing.
+ *  - Size limit: returns RK_ERR_WORKSPACE, before launching anything, when
+ *    rk_linear_logp_workspace_size(T, H, V) > 32 MiB (33554432 bytes), i.e.
+ *    about T * ceil(V/256) * 8 + T * 4 bytes; e.g. at most 8363 rows for
+ *    V = 128256 and 33420 rows for V = 32000.
+ *  - The first call on each device looks up that device's array address
+ *    (with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls on a device share the one array and nothing in it needs to
+ *    start at zero; calls that overlap on the GPU (several streams, or
+ *    several host threads at once) race on it and must be serialised.
+ */
+rk_status rk_linear_logp_noalloc(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                                 const int32_t *cu_seqlens, int32_t num_seqs,
+                                 int64_t T, int64_t H, int64_t V,
+                                 float *logp, float *lse, void *stream);
+
+/*
  * Reads and clears the device error word of the current device after
  * synchronising `stream`.  *err receives an OR of RK_DEVERR_* bits (0 = none).
  * For tests and debugging; it is the only call that synchronises.

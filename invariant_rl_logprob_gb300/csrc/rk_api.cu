@@ -73,6 +73,8 @@ bool encode_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t inner, uint
                      row_stride_bytes, box_inner, box_outer, sw128);
 }
 
+void record_cuda_error(int e) { g_last_cuda_error = e; }
+
 cudaError_t current_device_info(DeviceInfo *di) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -15,6 +15,9 @@ struct DeviceInfo {
     unsigned *err = nullptr;  // device address of this device's error word
 };
 
+// Records the CUDA error behind an RK_ERR_CUDA for rk_last_cuda_error().
+void record_cuda_error(int e);
+
 // Fills `di` for the current device (first call per device does the lookups).
 cudaError_t current_device_info(DeviceInfo *di);
 
