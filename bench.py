@@ -11,6 +11,11 @@ device time, inputs resident in HBM.  h (512 MB) and W (1.05 GB) exceed the
 126 MB L2, so nothing carries over between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    python bench.py --case {fwd,bwd,logits} [--shape T,H,V] [--reps R]
+
+`--case` runs one operator a few times on a small workload (for profiler
+captures; default T=2048, H=4096, V=32000: W and the logits exceed L2) and
+prints its mean device time.
 
 Under torchrun (N > 1) every rank runs its own group (weak scaling, no data
 collective); the timed region is bracketed by barriers and the max over ranks
@@ -112,7 +117,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -266,7 +271,7 @@ def run_gpu(args) -> None:
     ws_fwd = torch.empty(rk.linear_logp_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
     ws_bwd = torch.empty(rk.linear_logp_bwd_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
     bwd_chunks = 1   # the full workspace holds every row: one dZ GEMM + one dh GEMM
-    launches_per_step = 2 + (2 * bwd_chunks + 1) + 1
+    launches_per_step = 2 + (2 * bwd_chunks + 1) + 1   # fwd: 2, bwd: 3, logits: 1
 
     def step(i):
         rk.linear_logp(h, W, tg, out=logp, lse=lse, workspace=ws_fwd, stream=stream)
@@ -310,6 +315,22 @@ def run_gpu(args) -> None:
     err = rk.get_device_error(stream)
     if err:
         raise RuntimeError(f"device error word {err:#x} in the timed region")
+
+    # the logits path on its own: a loop over the rotated buffers (each call's
+    # input is absent from L2, and no dirty lines of the GEMMs are pending)
+    lg_reps = 50
+    for i in range(3):
+        z, zt = zs[i % len(zs)]
+        rk.logp_from_logits(z, zt, out=zlogp, lse=zlse, stream=stream)
+    ls0 = torch.cuda.Event(enable_timing=True)
+    ls1 = torch.cuda.Event(enable_timing=True)
+    ls0.record(stream)
+    for i in range(lg_reps):
+        z, zt = zs[i % len(zs)]
+        rk.logp_from_logits(z, zt, out=zlogp, lse=zlse, stream=stream)
+    ls1.record(stream)
+    torch.cuda.synchronize(dev)
+    lg_loop_ms = ls0.elapsed_time(ls1) / lg_reps
 
     ms_step_local = total_ms / args.steps
     ms_step = max_over_ranks(ms_step_local, ws)
@@ -365,7 +386,8 @@ def run_gpu(args) -> None:
     tc_tflops = (flops_fwd + flops_bwd) / ((fwd_ms + bwd_ms) / 1000.0) / 1e12
     peak_tc = peaks["bf16_tflops_sustained"]
     lg_bytes = Tl * Vl * 2 + Tl * 8 + 2 * Tl * 4
-    lg_gbs = lg_bytes / (lg_ms / 1000.0) / 1e9
+    lg_gbs = lg_bytes / (lg_loop_ms / 1000.0) / 1e9
+    lg_gbs_step = lg_bytes / (lg_ms / 1000.0) / 1e9
     traffic = None
     if TRAFFIC_RECORD["source_sha1"] == kernel_source_sha1():
         traffic = TRAFFIC_RECORD["fwd_tiles_bytes"]
@@ -396,12 +418,20 @@ def run_gpu(args) -> None:
         "bwd_tflops": flops_bwd / (bwd_ms / 1000.0) / 1e12,
         "logits_path": {"bound": "hbm", "achieved": lg_gbs, "peak": peaks["hbm_gbs"],
                         "unit": "GB/s", "frac": lg_gbs / peaks["hbm_gbs"],
-                        "bytes_per_call": lg_bytes, "us_per_call": lg_ms * 1000.0,
-                        "tokens_per_s": Tl / (lg_ms / 1000.0)},
+                        "bytes_per_call": lg_bytes, "us_per_call": lg_loop_ms * 1000.0,
+                        "tokens_per_s": Tl / (lg_loop_ms / 1000.0),
+                        "timing": f"{lg_reps} calls over {N_LOGITS_BUFFERS} rotated buffers "
+                                  "after the step loop (CUDA events, launching stream)",
+                        "in_step": {"us_per_call": lg_ms * 1000.0, "achieved": lg_gbs_step,
+                                    "frac": lg_gbs_step / peaks["hbm_gbs"],
+                                    "note": "measured right after the dh GEMM: its dirty L2 "
+                                            "lines are written back during this call"}},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches_note": f"{launches_per_step} librk kernels per step x {args.steps} steps "
+                             "in the timed region",
         "clocks": clocks,
         "wall_s_timed": wall,
         "device": torch.cuda.get_device_name(dev),
@@ -412,6 +442,51 @@ def run_gpu(args) -> None:
         dist.destroy_process_group()
 
 
+def run_case(args) -> None:
+    """One operator, a few launches, on a small workload (profiling)."""
+    import torch
+
+    import invariant_rl_logprob_gb300 as rk
+    from invariant_rl_logprob_gb300 import build as rk_build
+    from invariant_rl_logprob_gb300 import synth
+    rk_build.build()
+    dev = torch.device("cuda", 0)
+    T, H, V = (int(x) for x in args.shape.split(","))
+    if args.case == "logits":
+        z, tg, _ = synth.logits_batch(T=T, V=V)
+        z, tg = z.to(dev), tg.to(dev)
+        fn = lambda: rk.logp_from_logits(z, tg)
+        nbytes = T * V * 2 + T * 16
+        work = f"{nbytes / 1e6:.1f} MB"
+    else:
+        pool = synth.make_pool(H, V, [T], seed=4, with_grad=True)
+        h, W, tg, g = (pool.h.to(dev), pool.W.to(dev), pool.targets.to(dev), pool.g.to(dev))
+        _, lse = rk.linear_logp(h, W, tg)
+        if args.case == "fwd":
+            fn = lambda: rk.linear_logp(h, W, tg)
+            flops = 2.0 * T * H * V
+        else:
+            ws = torch.empty(rk.linear_logp_bwd_workspace_size(T, H, V), dtype=torch.uint8,
+                             device=dev)
+            fn = lambda: rk.linear_logp_bwd(h, W, tg, lse, g, workspace=ws)
+            flops = 4.0 * T * H * V
+        work = f"{flops / 1e12:.3f} TFLOP"
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.reps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / args.reps
+    if rk.get_device_error():
+        raise RuntimeError("device error word set")
+    print(json.dumps({"case": args.case, "shape": [T, H, V], "reps": args.reps,
+                      "ms_per_call": ms, "work": work}))
+
+
 def main() -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -420,7 +495,13 @@ def main() -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["fwd", "bwd", "logits"], default=None)
+    ap.add_argument("--shape", default="2048,4096,32000")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -8,24 +8,30 @@
 //
 // HBM-bound: every logit is read once (T*V*2 bytes), nothing else is large.
 //
-// Batch invariance by construction.  A row is reduced by one CTA; the columns
-// are cut into groups of 8 (group g = columns [8g, 8g+8)); thread i of the
-// CTA folds groups i, i+NT, i+2NT, ... in ascending order into a running
-// (max, sum-exp); the NT partials are merged by a fixed xor-shuffle tree and
-// a fixed cross-warp tree.  That order depends only on V -- never on T, the
-// row's index, the grid size or the row's address alignment: rows whose
-// address allows 16-byte loads use them, others load 2-byte elements, and both
-// evaluate exactly the same sequence of floating-point operations.
+// Batch invariance by construction.  A row is reduced by two warps, i.e. 64
+// "virtual lanes" vl = 32 * (warp of the row) + lane.  The columns are cut into
+// groups of 8 (group g = columns [8g, 8g+8)); virtual lane vl owns groups
+// vl, vl + 64, vl + 128, ... and folds them, in that order, in batches of 8
+// groups: the batch maximum (exact, any order) updates the running max once,
+// then the batch's 64 terms 2^((z - m) log2 e) are summed by a fixed pairwise
+// tree and added to the running sum.  The 32 partials of a warp are merged by a
+// fixed xor-shuffle tree, and the two warps' partials by one final merge.  All
+// of that depends only on V -- never on T, the row's index, the grid or the
+// row's address: rows whose address allows 16-byte loads use them, others load
+// 2-byte elements into the same groups (missing columns read as -inf) and run
+// exactly the same floating-point operations.
 #include "rk_device.cuh"
 #include "rk_internal.h"
 
 namespace rk {
 namespace {
 
-constexpr int kThreads = 256;           // threads per row (fixed for every T)
-constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 4;              // groups in flight per thread
-constexpr int kBlocksPerSm = 4;
+constexpr int kWarpsPerRow = 2;
+constexpr int kLanesPerRow = 32 * kWarpsPerRow;
+constexpr int kThreads = 128;
+constexpr int kRowsPerBlock = kThreads / kLanesPerRow;
+constexpr int kBatch = 8;  // groups per batch (64 values)
+constexpr uint32_t kNegInfPair = 0xFF80FF80u;  // two bf16 -inf
 
 __device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p) {
     uint4 v;
@@ -35,132 +41,125 @@ __device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p) {
     return v;
 }
 
-// Folds one group of 8 values (invalid columns hold -inf) into (m, s).
-__device__ __forceinline__ void fold_group(const float (&x)[8], float &m, float &s) {
-    float gm = x[0];
-#pragma unroll
-    for (int j = 1; j < 8; ++j) gm = fmaxf(gm, x[j]);
-    if (gm > m) {
-        // ex2((m - gm) * log2e) == 1 exactly when gm == m, so skipping the
-        // rescale when the maximum does not grow changes no bit.
-        s = __fmul_rn(s, ex2(__fmul_rn(__fsub_rn(m, gm), kLog2e)));
-        m = gm;
-    }
-    const float mb = __fmul_rn(-m, kLog2e);
-    float e[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) e[j] = ex2(__fmaf_rn(x[j], kLog2e, mb));
-    const float local = __fadd_rn(__fadd_rn(__fadd_rn(e[0], e[1]), __fadd_rn(e[2], e[3])),
-                                  __fadd_rn(__fadd_rn(e[4], e[5]), __fadd_rn(e[6], e[7])));
-    s = __fadd_rn(s, local);
+// Elementwise max of two bf16 pairs (exact).
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&x)[8]) {
-    x[0] = bf16_lo(v.x);
-    x[1] = bf16_hi(v.x);
-    x[2] = bf16_lo(v.y);
-    x[3] = bf16_hi(v.y);
-    x[4] = bf16_lo(v.z);
-    x[5] = bf16_hi(v.z);
-    x[6] = bf16_lo(v.w);
-    x[7] = bf16_hi(v.w);
+// Folds a batch of kBatch groups (8 bf16 each, packed as uint4) into (m, s).
+__device__ __forceinline__ void fold_batch(const uint4 (&w)[kBatch], float &m, float &s) {
+    uint32_t t[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+        t[u] = max_bf16x2(max_bf16x2(w[u].x, w[u].y), max_bf16x2(w[u].z, w[u].w));
+#pragma unroll
+    for (int st = 1; st < kBatch; st *= 2)
+#pragma unroll
+        for (int u = 0; u + st < kBatch; u += 2 * st) t[u] = max_bf16x2(t[u], t[u + st]);
+    const float bm = fmaxf(bf16_lo(t[0]), bf16_hi(t[0]));
+    if (bm > m) {
+        // ex2((m - bm) log2 e) == 1 exactly when bm == m, so skipping the
+        // rescale when the maximum does not grow changes no bit.
+        s = __fmul_rn(s, ex2(__fmul_rn(__fsub_rn(m, bm), kLog2e)));
+        m = bm;
+    }
+    const float mb = __fmul_rn(-m, kLog2e);
+    float l[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+        const uint32_t q[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+        float e[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            e[2 * j] = ex2(__fmaf_rn(bf16_lo(q[j]), kLog2e, mb));
+            e[2 * j + 1] = ex2(__fmaf_rn(bf16_hi(q[j]), kLog2e, mb));
+        }
+        l[u] = __fadd_rn(__fadd_rn(__fadd_rn(e[0], e[1]), __fadd_rn(e[2], e[3])),
+                         __fadd_rn(__fadd_rn(e[4], e[5]), __fadd_rn(e[6], e[7])));
+    }
+#pragma unroll
+    for (int st = 1; st < kBatch; st *= 2)
+#pragma unroll
+        for (int u = 0; u + st < kBatch; u += 2 * st) l[u] = __fadd_rn(l[u], l[u + st]);
+    s = __fadd_rn(s, l[0]);
+}
+
+// Group g of a row as 4 packed bf16 pairs, from 2-byte loads (-inf past V).
+__device__ __forceinline__ uint4 load_group_scalar(const uint16_t *zrow, int64_t g, int64_t V) {
+    uint32_t h[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int64_t c = (g << 3) + j;
+        h[j] = (c < V) ? (uint32_t)__ldg(zrow + c) : 0xFF80u;
+    }
+    return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                      h[6] | (h[7] << 16));
 }
 
 // VEC: 16-byte loads (V % 8 == 0 and a 16-byte aligned base); otherwise
 // 2-byte loads of the same groups.
 template <bool VEC>
-__global__ void __launch_bounds__(kThreads, kBlocksPerSm)
+__global__ void __launch_bounds__(kThreads)
     logits_logp_kernel(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targets,
                        const int32_t *__restrict__ cu, int num_seqs, int64_t T, int64_t V,
                        float *__restrict__ logp, float *__restrict__ lse, unsigned *err) {
-    __shared__ float sm_m[kWarps];
-    __shared__ float sm_s[kWarps];
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
+    __shared__ float sh_m[kThreads / 32], sh_s[kThreads / 32];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int wr = warp % kWarpsPerRow;
+    const int vl = wr * 32 + lane;
+    const int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + warp / kWarpsPerRow;
+    const int64_t tgt = (row < T) ? targets[row] : -1;
+    const bool active = row < T && row_active(row, tgt, cu, num_seqs);  // uniform per row
+    const uint16_t *zrow = logits + row * V;
     const int64_t G = (V + 7) >> 3;
 
-    for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
-        const int64_t tgt = targets[row];
-        const bool active = row_active(row, tgt, cu, num_seqs);
-        if (!active) {  // uniform across the block
-            if (tid == 0) {
-                logp[row] = 0.f;
-                if (lse) lse[row] = 0.f;
+    float m = -INFINITY, s = 0.f;
+    if (active) {
+        const int64_t n_i = (G - vl + kLanesPerRow - 1) / kLanesPerRow;  // groups of this lane
+        for (int64_t i0 = 0; i0 < n_i; i0 += kBatch) {
+            uint4 w[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int64_t i = i0 + u;
+                const int64_t g = vl + (int64_t)kLanesPerRow * i;
+                if (i < n_i)
+                    w[u] = VEC ? ld_stream_v4(reinterpret_cast<const uint4 *>(zrow) + g)
+                               : load_group_scalar(zrow, g, V);
+                else
+                    w[u] = make_uint4(kNegInfPair, kNegInfPair, kNegInfPair, kNegInfPair);
             }
-            continue;
+            fold_batch(w, m, s);
         }
-        const uint16_t *zrow = logits + row * V;
-        const bool tgt_ok = tgt < V;
-        float zt = 0.f;
-        if (tid == 0 && tgt_ok) zt = bf16_bits_to_f32(zrow[tgt]);
-
-        float m = -INFINITY, s = 0.f;
-        if (VEC) {
-            const uint4 *rv = reinterpret_cast<const uint4 *>(zrow);
-            for (int64_t g0 = tid; g0 < G; g0 += (int64_t)kThreads * kUnroll) {
-                uint4 v[kUnroll];
+    }
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int64_t g = g0 + (int64_t)u * kThreads;
-                    if (g < G) v[u] = ld_stream_v4(rv + g);
-                }
+    for (int off = 16; off > 0; off >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+        const float so = __shfl_xor_sync(0xffffffffu, s, off);
+        lse_merge(m, s, mo, so);
+    }
+    if (lane == 0) {
+        sh_m[warp] = m;
+        sh_s[warp] = s;
+    }
+    __syncthreads();
+    if (row < T && wr == 0 && lane == 0) {
+        if (!active) {
+            logp[row] = 0.f;
+            if (lse) lse[row] = 0.f;
+        } else if (tgt < V) {
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int64_t g = g0 + (int64_t)u * kThreads;
-                    if (g < G) {
-                        float x[8];
-                        unpack8(v[u], x);
-                        fold_group(x, m, s);
-                    }
-                }
-            }
+            for (int k = 1; k < kWarpsPerRow; ++k) lse_merge(m, s, sh_m[warp + k], sh_s[warp + k]);
+            const float l = __fadd_rn(m, logf(s));
+            logp[row] = __fsub_rn(bf16_bits_to_f32(zrow[tgt]), l);
+            if (lse) lse[row] = l;
         } else {
-            for (int64_t g = tid; g < G; g += kThreads) {
-                float x[8];
-                const int64_t c0 = g << 3;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int64_t c = c0 + j;
-                    x[j] = (c < V) ? bf16_bits_to_f32(__ldg(zrow + c)) : -INFINITY;
-                }
-                fold_group(x, m, s);
-            }
+            logp[row] = __int_as_float(0x7fc00000);
+            if (lse) lse[row] = __int_as_float(0x7fc00000);
+            atomicOr(err, kErrTargetRange);
         }
-
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-            const float so = __shfl_xor_sync(0xffffffffu, s, off);
-            lse_merge(m, s, mo, so);
-        }
-        if (lane == 0) {
-            sm_m[warp] = m;
-            sm_s[warp] = s;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            m = (lane < kWarps) ? sm_m[lane] : -INFINITY;
-            s = (lane < kWarps) ? sm_s[lane] : 0.f;
-#pragma unroll
-            for (int off = kWarps / 2; off > 0; off >>= 1) {
-                const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-                const float so = __shfl_xor_sync(0xffffffffu, s, off);
-                lse_merge(m, s, mo, so);
-            }
-            if (lane == 0) {
-                if (tgt_ok) {
-                    const float l = __fadd_rn(m, logf(s));
-                    logp[row] = __fsub_rn(zt, l);
-                    if (lse) lse[row] = l;
-                } else {
-                    logp[row] = __int_as_float(0x7fc00000);
-                    if (lse) lse[row] = __int_as_float(0x7fc00000);
-                    atomicOr(err, kErrTargetRange);
-                }
-            }
-        }
-        __syncthreads();  // sm_m / sm_s are reused by the next row
     }
 }
 
@@ -170,8 +169,7 @@ cudaError_t launch_logits_logp(const uint16_t *logits, const int64_t *targets, c
                                int num_seqs, int64_t T, int64_t V, float *logp, float *lse,
                                const DeviceInfo &di, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
-    const int64_t max_grid = (int64_t)di.sm_count * kBlocksPerSm;
-    const unsigned grid = (unsigned)(T < max_grid ? T : max_grid);
+    const unsigned grid = (unsigned)((T + kRowsPerBlock - 1) / kRowsPerBlock);
     const bool vec = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
     if (vec)
         logits_logp_kernel<true><<<grid, kThreads, 0, st>>>(logits, targets, cu, num_seqs, T, V,
