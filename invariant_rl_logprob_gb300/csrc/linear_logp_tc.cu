@@ -11,15 +11,21 @@
 //   dZ[t, v] = g[t] exp(z[t, v] - lse[t])                     (GEMM 1, stored bf16)
 //   dh[t, :] = g[t] W[target_t, :] - sum_v dZ[t, v] W[v, :]    (GEMM 2, fp32)
 //
-// One persistent, warp-specialised tile kernel serves the three GEMMs:
-//   warp 4      TMA producer: 128x64 tiles of A and 256x64 (K-major) or 64x256
-//               (MN-major) tiles of B through a 4-stage shared-memory ring,
-//               128-byte swizzle;
-//   warp 5      allocates 512 TMEM columns and issues tcgen05.mma (M=128,
-//               N=256, K=16, bf16 x bf16 -> fp32) into one of two 256-column
-//               accumulators;
-//   warps 0-3   epilogue: thread i owns tile row i (TMEM lane i) and drains the
-//               other accumulator while the next tile accumulates.
+// One persistent, warp-specialised tile kernel serves the three GEMMs.  It
+// runs as CTA pairs (clusters of 2 on neighbouring SMs) sharing 256x256 output
+// tiles through the pair form of the tensor core (tcgen05 cta_group::2):
+//   warp 4      TMA producer (both CTAs): this CTA's 128 rows of A and 128 of
+//               the tile's 256 B rows (K-major 128x64, or two MN-major 64x64
+//               boxes) per 64-wide K stage, 6-stage ring, 128-byte swizzle;
+//               all copies of a stage complete on the even CTA's barrier;
+//   warp 5      allocates 512 TMEM columns (both CTAs, collectively); in the
+//               even CTA, issues tcgen05.mma (M=256, N=256, K=16, bf16 x bf16
+//               -> fp32) into one of two 256-column accumulators, reading A and
+//               B from both CTAs' shared memory and writing each CTA's 128
+//               rows of D to its own TMEM; commits signal both CTAs;
+//   warps 0-3   epilogue (both CTAs): thread i owns row i of its CTA's half
+//               (TMEM lane i) and drains one accumulator while the next tile
+//               accumulates into the other.
 // Epilogues:
 //   kFwd  the row's softmax partial over the tile's 256 vocabulary columns,
 //         m = max z, s = sum 2^((z - m) log2 e), and z[target] if the target
@@ -44,13 +50,13 @@
 namespace rk {
 namespace {
 
-constexpr int BM = 128;  // tile rows (TMEM lanes)
-constexpr int BN = 256;  // tile columns (TMEM columns per accumulator)
+constexpr int BM = 128;  // tile rows per CTA (TMEM lanes); a pair covers 2*BM
+constexpr int BN = 256;  // tile columns (TMEM columns per accumulator); each CTA stages BN/2 B rows
 constexpr int BK = 64;   // K per pipeline stage (64 bf16 = one 128-byte swizzle row)
 constexpr int UK = 16;   // K per tcgen05.mma of kind::f16
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kABytes = BM * BK * 2;
-constexpr int kBBytes = BN * BK * 2;
+constexpr int kBBytes = (BN / 2) * BK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * BN;
 constexpr int kEpiThreads = 128;
@@ -61,6 +67,8 @@ constexpr int kGroupN = 16;  // raster group (in N tiles) of the forward / dZ GE
 
 enum Mode { kFwd = 0, kDz = 1, kDh = 2 };
 
+// full / tmem_empty / drain are used in the even CTA only; empty and
+// tmem_full in both (the MMA commits are multicast to the pair).
 struct Ctl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
@@ -81,7 +89,7 @@ struct TileArgs {
     int64_t row0;
     int64_t rows;  // rows of this launch (local)
     int32_t V;
-    int32_t num_m, num_n, num_k;
+    int32_t num_m, num_n, num_k;  // num_m counts 256-row pair tiles
     unsigned *err;
     // kFwd
     float2 *part;  // [rows][num_n]
@@ -124,13 +132,13 @@ __device__ __forceinline__ void tile_coords(int64_t tile, const TileArgs &a, int
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     linear_logp_tiles(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const TileArgs a) {
     // kDh: B is W read as [K = vocabulary rows, N = H columns] (N contiguous,
-    // "MN-major"), staged as four 64-column boxes of BK rows each.
+    // "MN-major"), staged as two 64-column boxes of BK rows per CTA.
     constexpr bool kBmn = (MODE == kDh);
-    constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, false, kBmn);
+    constexpr uint32_t kIdesc = idesc_bf16_f32(2 * BM, BN, false, kBmn);
     constexpr uint32_t kBBoxBytes = BK * 64 * 2;  // one 64-column MN-major box
     // Descriptor strides.  K-major, 128B swizzle: 8-row groups 1024 B apart;
     // the next 16-wide K slice starts 32 B further.  MN-major, 128B swizzle:
@@ -146,6 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+    const int64_t pair = blockIdx.x >> 1;
+    const int64_t npairs = gridDim.x >> 1;
     const int64_t total = (int64_t)a.num_m * a.num_n;
 
     if (threadIdx.x == 0) {
@@ -155,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->tmem_full[b]), 1);
-            mbar_init(smem_u32(&ctl->tmem_empty[b]), kEpiThreads);
+            mbar_init(smem_u32(&ctl->tmem_empty[b]), 2 * (kEpiThreads / 32));
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort = 0;
@@ -166,11 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmB);
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(smem_u32(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // both CTAs' barriers initialised, TMEM allocated
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort = &ctl->abort;
@@ -186,29 +198,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 last_ph[i] = 0;
             }
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int64_t tile = pair; tile < total && ok; tile += npairs) {
                 int mb, nb;
                 tile_coords<MODE>(tile, a, mb, nb);
+                const int arow = mb * 2 * BM + (int)rank * BM;     // this CTA's A rows
+                const int bn0 = nb * BN + (int)rank * (BN / 2);    // this CTA's B rows / H columns
+                int nbox0 = 0, nbox1 = 0;
+                if constexpr (kBmn) {
+                    nbox0 = max(0, min(2, (a.H - nb * BN) / 64));
+                    nbox1 = max(0, min(2, (a.H - nb * BN - BN / 2) / 64));
+                }
                 for (int kb = 0; kb < a.num_k; ++kb) {
                     if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort, a.err)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_u32(&ctl->full[s]);
+                    const uint32_t fb = mapa_shared(smem_u32(&ctl->full[s]), 0);
                     const uint32_t sa = sbase + (uint32_t)(s * kStageBytes);
+                    if (rank == 0) {
+                        const uint32_t bytes = kBmn ? (uint32_t)(2 * kABytes + (nbox0 + nbox1) * (int)kBBoxBytes)
+                                                    : (uint32_t)(2 * kStageBytes);
+                        mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), bytes);
+                    }
+                    tma_load_2d_pair(sa, &tmA, fb, kb * BK, arow);
                     if constexpr (kBmn) {
-                        // only the 64-column boxes that start inside H are loaded; the
-                        // accumulator columns of the others are never stored
-                        const int nbox = min(BN / 64, (a.H - nb * BN) / 64);
-                        mbar_arrive_expect_tx(fb, (uint32_t)(kABytes + nbox * (int)kBBoxBytes));
-                        tma_load_2d(sa, &tmA, fb, kb * BK, mb * BM);
+                        const int nbox = rank == 0 ? nbox0 : nbox1;
                         for (int j = 0; j < nbox; ++j)
-                            tma_load_2d(sa + kABytes + j * kBBoxBytes, &tmB, fb, nb * BN + j * 64,
-                                        kb * BK);
+                            tma_load_2d_pair(sa + kABytes + j * kBBoxBytes, &tmB, fb, bn0 + j * 64,
+                                             kb * BK);
                     } else {
-                        mbar_arrive_expect_tx(fb, kStageBytes);
-                        tma_load_2d(sa, &tmA, fb, kb * BK, mb * BM);
-                        tma_load_2d(sa + kABytes, &tmB, fb, kb * BK, nb * BN);
+                        tma_load_2d_pair(sa + kABytes, &tmB, fb, kb * BK, bn0);
                     }
                     used[s] = true;
                     last_ph[s] = ph;
@@ -218,19 +237,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!ok) {  // let every issued copy land before the block exits
-                for (int i = 0; i < kStages; ++i)
-                    if (used[i]) mbar_wait_drain(smem_u32(&ctl->full[i]), last_ph[i], 100000000ull);
+            if (!ok) {  // let every issued copy land before the pair exits
+                if (rank == 0) {
+                    for (int i = 0; i < kStages; ++i)
+                        if (used[i])
+                            mbar_wait_drain(smem_u32(&ctl->full[i]), last_ph[i], 100000000ull);
+                } else {
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 2000000ull) {
+                    }
+                }
             }
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             int s = 0;
             uint32_t ph = 0;
             int b = 0;
             uint32_t tph = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int64_t tile = pair; tile < total && ok; tile += npairs) {
                 if (!mbar_wait(smem_u32(&ctl->tmem_empty[b]), tph ^ 1u, abort, a.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(b * BN);
@@ -245,41 +271,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd = smem_desc_sw128(sa + kABytes, kBLbo, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BK / UK; ++kk) {
-                        mma_bf16_ss(d, ad + (uint64_t)((kk * UK * 2) >> 4),
-                                    bd + (uint64_t)((kk * kBStepK) >> 4), kIdesc,
-                                    (kb | kk) != 0 ? 1u : 0u);
+                        mma_bf16_ss_pair(d, ad + (uint64_t)((kk * UK * 2) >> 4),
+                                         bd + (uint64_t)((kk * kBStepK) >> 4), kIdesc,
+                                         (kb | kk) != 0 ? 1u : 0u);
                     }
-                    mma_commit(smem_u32(&ctl->empty[s]));
+                    mma_commit_pair(smem_u32(&ctl->empty[s]), 0x3);
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&ctl->tmem_full[b]));
+                mma_commit_pair(smem_u32(&ctl->tmem_full[b]), 0x3);
                 if (++b == 2) {
                     b = 0;
                     tph ^= 1u;
                 }
             }
-            // No MMA may still be writing TMEM when the block releases it.
-            mma_commit(smem_u32(&ctl->drain));
+            // No MMA may still be reading shared memory or writing TMEM when
+            // the pair releases them.
+            mma_commit_pair(smem_u32(&ctl->drain), 0x1);
             mbar_wait_drain(smem_u32(&ctl->drain), 0, 1000000000ull);
         }
     } else {
-        // Epilogue: warp w reads TMEM lanes [32w, 32w+32) = tile rows.
+        // Epilogue: warp w reads TMEM lanes [32w, 32w+32) = rows of this CTA's half.
         int b = 0;
         uint32_t tph = 0;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        for (int64_t tile = pair; tile < total; tile += npairs) {
             int mb, nb;
             tile_coords<MODE>(tile, a, mb, nb);
-            const int64_t lrow = (int64_t)mb * BM + threadIdx.x;  // local row
+            const int64_t lrow = (int64_t)mb * 2 * BM + (int64_t)rank * BM + threadIdx.x;  // local row
             const bool in_range = lrow < a.rows;
             const int64_t grow = a.row0 + lrow;                    // global row
             const int64_t tgt = in_range ? a.targets[grow] : -1;
             const int n0 = nb * BN;
-
+            const uint32_t empty_bar = mapa_shared(smem_u32(&ctl->tmem_empty[b]), 0);
             if constexpr (MODE == kFwd) {
                 const int valid = min(BN, a.V - n0);
                 const int tcol = (tgt >= n0 && tgt < (int64_t)n0 + valid) ? (int)(tgt - n0) : -1;
@@ -339,7 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float s = __fadd_rn(__fadd_rn(acc0, acc1), __fadd_rn(acc2, acc3));
                 tc_fence_before();
-                mbar_arrive(smem_u32(&ctl->tmem_empty[b]));
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(empty_bar);
                 if (in_range) {
                     a.part[lrow * a.num_n + nb] = make_float2(m, s);
                     if (tcol >= 0) a.ztgt[lrow] = zt;
@@ -383,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(smem_u32(&ctl->tmem_empty[b]));
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(empty_bar);
             } else {  // kDh
                 const bool active = in_range && row_active(grow, tgt, a.cu, a.num_seqs) && tgt < a.V;
                 const float g = active ? a.grad[grow] : 0.f;
@@ -426,7 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(smem_u32(&ctl->tmem_empty[b]));
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(empty_bar);
             }
             if (++b == 2) {
                 b = 0;
@@ -437,10 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // the pair is done with its shared memory and TMEM
     if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc_pair(tmem, kTmemCols);
     }
 }
 
@@ -515,6 +546,26 @@ cudaError_t set_smem_attr(const DeviceInfo &di) {
     return e;
 }
 
+// CTA pairs that can be resident at once (the persistent grid never exceeds it).
+template <int MODE>
+int64_t resident_pairs(const DeviceInfo &di) {
+    static thread_local int dev = -1;
+    static thread_local int64_t val = 0;
+    if (dev == di.device) return val;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * (di.sm_count / 2)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, linear_logp_tiles<MODE>, &cfg) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        n = di.sm_count / 2;
+    }
+    val = std::min<int64_t>(n, di.sm_count / 2);
+    dev = di.device;
+    return val;
+}
+
 template <int MODE>
 cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const TileArgs &a,
                       const DeviceInfo &di, cudaStream_t st) {
@@ -522,7 +573,8 @@ cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tile
     if (e != cudaSuccess) return e;
     const int64_t tiles = (int64_t)a.num_m * a.num_n;
     if (tiles == 0) return cudaSuccess;
-    const unsigned grid = (unsigned)std::min<int64_t>(tiles, di.sm_count);
+    const int64_t pairs = std::min<int64_t>(tiles, resident_pairs<MODE>(di));
+    const unsigned grid = (unsigned)(2 * pairs);
     linear_logp_tiles<MODE><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, a);
     return cudaGetLastError();
 }
@@ -545,7 +597,7 @@ cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_
     CUtensorMap tmA, tmB;
     if (!encode_tmap_bf16_2d(&tmA, h, (uint64_t)H, (uint64_t)T, (uint64_t)H * 2, BK, BM, true))
         return cudaErrorInvalidValue;
-    if (!encode_tmap_bf16_2d(&tmB, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN, true))
+    if (!encode_tmap_bf16_2d(&tmB, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2, true))
         return cudaErrorInvalidValue;
 
     TileArgs a{};
@@ -556,7 +608,7 @@ cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_
     a.rows = T;
     a.V = (int32_t)V;
     a.H = (int32_t)H;
-    a.num_m = (int32_t)((T + BM - 1) / BM);
+    a.num_m = (int32_t)((T + 2 * BM - 1) / (2 * BM));
     a.num_n = (int32_t)((V + BN - 1) / BN);
     a.num_k = (int32_t)(H / BK);
     a.err = di.err;
@@ -592,7 +644,7 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
     uint16_t *dz = reinterpret_cast<uint16_t *>(workspace);
 
     CUtensorMap tmW_k, tmW_mn;
-    if (!encode_tmap_bf16_2d(&tmW_k, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN, true))
+    if (!encode_tmap_bf16_2d(&tmW_k, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2, true))
         return cudaErrorInvalidValue;
     if (!encode_tmap_bf16_2d(&tmW_mn, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, 64, BK, true))
         return cudaErrorInvalidValue;
@@ -622,7 +674,7 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
         a.ldz = ldz;
         a.W = W;
         a.dh = dh;
-        a.num_m = (int32_t)((rows + BM - 1) / BM);
+        a.num_m = (int32_t)((rows + 2 * BM - 1) / (2 * BM));
 
         // GEMM 1: z recomputed, dZ = g exp(z - lse) in bf16
         a.num_n = (int32_t)((V + BN - 1) / BN);
