@@ -178,6 +178,16 @@ rk_status rk_linear_logp_noalloc(const uint16_t *h, const uint16_t *W, const int
  */
 rk_status rk_get_device_error(void *stream, int32_t *err);
 
+/*
+ * Self-test of the failure path that every pipeline wait in the library
+ * shares: one kernel waits on an mbarrier that is never completed, gives up
+ * after `limit_ns` (1 ns .. 10 s) and sets RK_DEVERR_TIMEOUT in the device
+ * error word, leaving the context usable.  (The pages' issue #244, #150
+ * "Silent fallback ... = fail": a stalled pipeline must surface as an error,
+ * never as a hang.)  Asynchronous; read the result with rk_get_device_error.
+ */
+rk_status rk_selftest_wait_timeout(int64_t limit_ns, void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *rk_status_string(rk_status s);
 

@@ -27,7 +27,7 @@ __all__ = [
     "linear_logp", "linear_logp_workspace_size",
     "logp_from_logits",
     "linear_logp_bwd", "linear_logp_bwd_workspace_size", "linear_logp_bwd_min_workspace_size",
-    "get_device_error", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT",
+    "get_device_error", "selftest_wait_timeout", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -77,6 +77,8 @@ def load_library() -> ctypes.CDLL:
     lib.rk_linear_logp_bwd_min_workspace_size.restype = sz
     lib.rk_linear_logp_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, sz, vp]
     lib.rk_linear_logp_bwd.restype = ctypes.c_int
+    lib.rk_selftest_wait_timeout.argtypes = [i64, vp]
+    lib.rk_selftest_wait_timeout.restype = ctypes.c_int
     lib.rk_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     lib.rk_get_device_error.restype = ctypes.c_int
     lib.rk_status_string.argtypes = [ctypes.c_int]
@@ -211,6 +213,13 @@ def linear_logp_bwd(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, lse
                                 workspace.numel(), _stream_handle(stream, h.device))
     _check(st, "rk_linear_logp_bwd")
     return dh
+
+
+def selftest_wait_timeout(limit_ns: int, stream: torch.cuda.Stream | None = None) -> None:
+    """Launch a kernel whose bounded wait must time out after ``limit_ns``."""
+    lib = load_library()
+    _check(lib.rk_selftest_wait_timeout(int(limit_ns), _stream_handle(stream, None)),
+           "rk_selftest_wait_timeout")
 
 
 def get_device_error(stream: torch.cuda.Stream | None = None) -> int:

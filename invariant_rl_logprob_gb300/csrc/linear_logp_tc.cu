@@ -64,6 +64,7 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kThreads = kEpiThreads + 64;
 constexpr int kGroupN = 16;  // raster group (in N tiles) of the forward / dZ GEMMs
+constexpr int kGroupNDh = 16;  // raster group (in H tiles) of the dh GEMM
 
 enum Mode { kFwd = 0, kDz = 1, kDh = 2 };
 
@@ -116,10 +117,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 template <int MODE>
 __device__ __forceinline__ void tile_coords(int64_t tile, const TileArgs &a, int &mb, int &nb) {
     if constexpr (MODE == kDh) {
-        // every H tile of a row block before the next row block: CTAs running
-        // together share A (dZ rows) and walk W's K (vocabulary) rows in step
-        mb = (int)(tile / a.num_n);
-        nb = (int)(tile - (int64_t)mb * a.num_n);
+        // groups of kGroupNDh H tiles; inside a group, row blocks outer: CTAs
+        // running together share A (dZ rows) and walk W's K (vocabulary) rows
+        // in step
+        const int64_t per_group = (int64_t)a.num_m * kGroupNDh;
+        const int64_t g = tile / per_group;
+        const int64_t r = tile - g * per_group;
+        const int n0 = (int)g * kGroupNDh;
+        const int gn = min(kGroupNDh, a.num_n - n0);
+        mb = (int)(r / gn);
+        nb = n0 + (int)(r % gn);
     } else {
         const int64_t per_group = (int64_t)a.num_m * kGroupN;
         const int64_t g = tile / per_group;
@@ -220,13 +227,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                                     : (uint32_t)(2 * kStageBytes);
                         mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), bytes);
                     }
-                    tma_load_2d_pair(sa, &tmA, fb, kb * BK, arow);
                     if constexpr (kBmn) {
+                        tma_load_2d_pair(sa, &tmA, fb, kb * BK, arow);
                         const int nbox = rank == 0 ? nbox0 : nbox1;
                         for (int j = 0; j < nbox; ++j)
                             tma_load_2d_pair(sa + kABytes + j * kBBoxBytes, &tmB, fb, bn0 + j * 64,
                                              kb * BK);
                     } else {
+                        tma_load_2d_pair(sa, &tmA, fb, kb * BK, arow);
                         tma_load_2d_pair(sa + kABytes, &tmB, fb, kb * BK, bn0);
                     }
                     used[s] = true;

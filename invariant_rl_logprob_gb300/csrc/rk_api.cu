@@ -6,7 +6,8 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/rk.h"
+#include "rk.h"
+#include "rk_device.cuh"
 #include "rk_internal.h"
 
 // One error word per device (the module is loaded per device context).
@@ -107,6 +108,19 @@ cudaError_t current_device_info(DeviceInfo *di) {
 using rk::DeviceInfo;
 
 namespace {
+
+// One thread waits on an mbarrier that nothing ever arrives on, through the
+// same bounded wait the pipelines use; it gives up after `limit_ns`.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned *err) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        rk::mbar_init(rk::smem_u32(&bar), 1);
+        abort_flag = 0;
+        rk::fence_mbar_init();
+        (void)rk::mbar_wait_limit(rk::smem_u32(&bar), 0, &abort_flag, err, limit_ns);
+    }
+}
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -217,6 +231,17 @@ rk_status rk_linear_logp_bwd(const uint16_t *h, const uint16_t *W, const int64_t
     if (e != cudaSuccess) return rk::cuda_fail(e);
     e = rk::launch_linear_bwd(h, W, targets, cu_seqlens, num_seqs, T, H, V, lse, grad_logp, dh,
                               workspace, workspace_bytes, di, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    return RK_OK;
+}
+
+rk_status rk_selftest_wait_timeout(int64_t limit_ns, void *stream) {
+    if (limit_ns <= 0 || limit_ns > 10000000000ll) return RK_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>((uint64_t)limit_ns, di.err);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return rk::cuda_fail(e);
     return RK_OK;
 }

@@ -120,21 +120,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Waits until the phase of `bar` with the given parity has completed.
 // Bounded: returns false (after raising *abort and the device error word) if
 // the wait exceeds kWaitLimitNs or another role of the block already aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          unsigned *err) {
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, volatile int *abort,
+                                                unsigned *err, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 atomicOr(err, kErrTimeout);
                 return false;
             }
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          unsigned *err) {
+    return mbar_wait_limit(bar, parity, abort, err, kWaitLimitNs);
 }
 
 // Same, without the abort protocol: used only for short drains on the abort path.

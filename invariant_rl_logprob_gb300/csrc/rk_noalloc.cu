@@ -12,7 +12,7 @@
 // The kernels are the same as rk_linear_logp's, so the results are identical.
 #include <mutex>
 
-#include "../../include/rk.h"
+#include "rk.h"
 #include "rk_internal.h"
 
 namespace {

@@ -66,6 +66,15 @@ def _load():
         lib.oracle_logp_from_logits.restype = i32
         lib.oracle_linear_logp_bwd.argtypes = [vp, i32, vp, i32, vp, vp, vp, i64, i64, i64, vp]
         lib.oracle_linear_logp_bwd.restype = i32
+        lib.oracle_lm_head.argtypes = [vp, i32, vp, i32, vp, i64, i64, i64, vp]
+        lib.oracle_lm_head.restype = i32
+        lib.oracle_logits_bwd.argtypes = [vp, i32, vp, vp, vp, i64, i64, vp]
+        lib.oracle_logits_bwd.restype = i32
+        d = ctypes.c_double
+        lib.oracle_grpo_token.argtypes = [vp, vp, vp, vp, i64, d, d, d, d, vp, vp, vp, vp]
+        lib.oracle_grpo_token.restype = None
+        lib.oracle_linear_greedy.argtypes = [vp, i32, vp, i32, vp, i64, i64, i64, vp, vp, vp]
+        lib.oracle_linear_greedy.restype = i32
         _lib = lib
     return _lib
 
@@ -171,6 +180,82 @@ def linear_logp_bwd(h, W, targets, grad_logp, cu_seqlens=None, rows=None):
             raise ValueError("oracle_linear_logp_bwd: target out of range or out of memory")
         dh[act] = out
     return dh
+
+
+def lm_head(h, W, rows=None) -> np.ndarray:
+    """z = h W^T in float64 for the selected rows: [n_rows, V] (no rounding)."""
+    h, hk = _as_matrix(h)
+    W, wk = _as_matrix(W)
+    T, H = h.shape
+    V = W.shape[0]
+    rows = np.arange(T, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    z = np.empty((rows.size, V), dtype=np.float64)
+    if rows.size and _load().oracle_lm_head(_ptr(h), hk, _ptr(W), wk, _ptr(rows), rows.size,
+                                            H, V, _ptr(z)) != 0:
+        raise MemoryError("oracle_lm_head")
+    return z
+
+
+def logits_bwd(logits, targets, grad_logp, cu_seqlens=None, rows=None) -> np.ndarray:
+    """d(g * logp)/d logits = g * (onehot - softmax) in float64, [n_rows, V];
+    zero rows for inactive tokens."""
+    z, zk = _as_matrix(logits)
+    targets = np.ascontiguousarray(targets, dtype=np.int64)
+    g = np.ascontiguousarray(grad_logp, dtype=np.float64)
+    T, V = z.shape
+    rows, act = _rows_to_run(targets, cu_seqlens, rows)
+    out = np.zeros((rows.shape[0], V), dtype=np.float64)
+    run = np.ascontiguousarray(rows[act])
+    if run.size:
+        o = np.empty((run.size, V), dtype=np.float64)
+        if _load().oracle_logits_bwd(_ptr(z), zk, _ptr(targets), _ptr(g), _ptr(run), run.size,
+                                     V, _ptr(o)) != 0:
+            raise ValueError("oracle_logits_bwd: target out of range or out of memory")
+        out[act] = o
+    return out
+
+
+def grpo_token(logp, logp_old, adv, logp_ref=None, targets=None, cu_seqlens=None, *,
+               eps_low=0.2, eps_high=0.2, beta=0.0, scale=1.0):
+    """Per-token GRPO loss: dict of float64 arrays loss, grad, ratio, kl
+    (zeros on inactive tokens; all tokens active when targets is None)."""
+    logp = np.ascontiguousarray(logp, dtype=np.float64)
+    n = logp.shape[0]
+    lo = np.ascontiguousarray(logp_old, dtype=np.float64)
+    a = np.ascontiguousarray(adv, dtype=np.float64)
+    ref = None if logp_ref is None else np.ascontiguousarray(logp_ref, dtype=np.float64)
+    act = np.ones(n, dtype=bool) if targets is None else active_rows(targets, cu_seqlens, n)
+    out = {k: np.zeros(n, dtype=np.float64) for k in ("loss", "grad", "ratio", "kl")}
+    idx = np.nonzero(act)[0]
+    if idx.size:
+        x_lp = np.ascontiguousarray(logp[idx])
+        x_lo = np.ascontiguousarray(lo[idx])
+        x_a = np.ascontiguousarray(a[idx])
+        x_ref = np.ascontiguousarray(ref[idx]) if ref is not None else None
+        o = {k: np.empty(idx.size, dtype=np.float64) for k in out}
+        _load().oracle_grpo_token(_ptr(x_lp), _ptr(x_lo),
+                                  _ptr(x_ref) if x_ref is not None else None, _ptr(x_a), idx.size,
+                                  eps_low, eps_high, beta, scale, _ptr(o["loss"]),
+                                  _ptr(o["grad"]), _ptr(o["ratio"]), _ptr(o["kl"]))
+        for k in out:
+            out[k][idx] = o[k]
+    return out
+
+
+def linear_greedy(h, W, rows=None):
+    """(token int64, logp float64, zmax float64) of the greedy step per row."""
+    h, hk = _as_matrix(h)
+    W, wk = _as_matrix(W)
+    T, H = h.shape
+    V = W.shape[0]
+    rows = np.arange(T, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    tok = np.empty(rows.size, dtype=np.int64)
+    lp = np.empty(rows.size, dtype=np.float64)
+    zm = np.empty(rows.size, dtype=np.float64)
+    if rows.size and _load().oracle_linear_greedy(_ptr(h), hk, _ptr(W), wk, _ptr(rows), rows.size,
+                                                  H, V, _ptr(tok), _ptr(lp), _ptr(zm)) != 0:
+        raise MemoryError("oracle_linear_greedy")
+    return tok, lp, zm
 
 
 def bf16_bits_to_f64(bits) -> np.ndarray:

@@ -216,3 +216,138 @@ int oracle_linear_logp_bwd(const void *h, int h_kind, const void *W, int w_kind,
     free(z);
     return rc;
 }
+
+/*
+ * lm_head on the listed rows: z[i, v] = sum_k h[r,k] W[v,k] in fp64 (the
+ * dense path's logits before any rounding; chain index 6 "lm_head" of PR #264
+ * "docs(ws1): batch-invariance contract RFC").  z: [n_rows, V].
+ */
+int oracle_lm_head(const void *h, int h_kind, const void *W, int w_kind,
+                   const int64_t *rows, int64_t n_rows, int64_t H, int64_t V, double *z)
+{
+    double *hrow = (double *)malloc(sizeof(double) * (size_t)(H > 0 ? H : 1));
+    if (!hrow)
+        return -1;
+    for (int64_t i = 0; i < n_rows; ++i)
+        logits_of_row(h, h_kind, rows[i], W, w_kind, H, V, hrow, z + i * V);
+    free(hrow);
+    return 0;
+}
+
+/*
+ * Logits-path backward on the listed rows: the gradient of g * logp with
+ * respect to the logits, dz[i, v] = g[r] * (onehot(target_r)[v] - p[v]),
+ * p = softmax(logits[r, :]) (the "dense vs indexed selected-logprob paths" of
+ * issue #101 "[RFC] Batch-Invariant RL Kernel Suite ...", Scope, with the
+ * backward made first-class in issue #244, Workstream 3).  dz: [n_rows, V].
+ */
+int oracle_logits_bwd(const void *logits, int kind, const int64_t *targets,
+                      const double *grad_logp, const int64_t *rows, int64_t n_rows,
+                      int64_t V, double *dz)
+{
+    double *z = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    if (!z)
+        return -1;
+    int rc = 0;
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const int64_t r = rows[i];
+        const int64_t t = targets[r];
+        if (t < 0 || t >= V) {
+            rc = -1;
+            break;
+        }
+        for (int64_t v = 0; v < V; ++v)
+            z[v] = elem(logits, kind, r * V + v);
+        const double l = log_sum_exp(z, V);
+        const double g = grad_logp[r];
+        for (int64_t v = 0; v < V; ++v)
+            dz[i * V + v] = g * ((v == t ? 1.0 : 0.0) - exp(z[v] - l));
+    }
+    free(z);
+    return rc;
+}
+
+/*
+ * Per-token GRPO loss ("grpo_loss, ratio_kl", issue #101 P0 list; chain index
+ * 9 of PR #264).  The pages name the operator, not its formula; this is the
+ * clipped-surrogate objective with a KL penalty to a reference policy, per
+ * token (no batch-level normalisation; a caller-given scale multiplies it):
+ *   ratio = exp(logp - logp_old)
+ *   surr  = min(ratio * A, clip(ratio, 1 - eps_low, 1 + eps_high) * A)
+ *   kl    = exp(logp_ref - logp) - (logp_ref - logp) - 1     (0 without logp_ref)
+ *   loss  = scale * (-surr + beta * kl)
+ *   grad  = d loss / d logp
+ *         = scale * (-A * ratio * [unclipped term selected or ratio inside the
+ *                                  clip range] + beta * (1 - exp(logp_ref - logp)))
+ * where the unclipped term is selected when ratio * A <= clip(ratio) * A.
+ * All n elements (the caller passes only active tokens).
+ */
+void oracle_grpo_token(const double *logp, const double *logp_old, const double *logp_ref,
+                       const double *adv, int64_t n, double eps_low, double eps_high,
+                       double beta, double scale, double *loss, double *grad,
+                       double *ratio_out, double *kl_out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const double ratio = exp(logp[i] - logp_old[i]);
+        const double a = adv[i];
+        const double lo = 1.0 - eps_low, hi = 1.0 + eps_high;
+        const double clipped = ratio < lo ? lo : (ratio > hi ? hi : ratio);
+        const double s1 = ratio * a, s2 = clipped * a;
+        const double surr = s1 <= s2 ? s1 : s2;
+        /* d surr / d logp: ratio * a through the unclipped term; through the
+         * clipped term only while ratio is inside [lo, hi] (there it equals s1) */
+        double dsurr;
+        if (s1 <= s2)
+            dsurr = ratio * a;
+        else
+            dsurr = (ratio > lo && ratio < hi) ? ratio * a : 0.0;
+        double kl = 0.0, dkl = 0.0;
+        if (logp_ref) {
+            const double d = logp_ref[i] - logp[i];
+            const double e = exp(d);
+            kl = e - d - 1.0;
+            dkl = 1.0 - e;
+        }
+        loss[i] = scale * (-surr + beta * kl);
+        grad[i] = scale * (-dsurr + beta * dkl);
+        if (ratio_out)
+            ratio_out[i] = ratio;
+        if (kl_out)
+            kl_out[i] = kl;
+    }
+}
+
+/*
+ * Greedy decoding step on the listed rows: the token with the largest logit
+ * z = h . W^T (the lowest index among equal maxima) and its logprob
+ * z[token] - logsumexp(z).  This is the decode side of issue #244, Workstream 2
+ * (#152 "Generate-then-re-score"): a later prefill scoring of the same tokens
+ * must give the same selected logprobs.
+ */
+int oracle_linear_greedy(const void *h, int h_kind, const void *W, int w_kind,
+                         const int64_t *rows, int64_t n_rows, int64_t H, int64_t V,
+                         int64_t *token, double *logp, double *zmax)
+{
+    double *hrow = (double *)malloc(sizeof(double) * (size_t)(H > 0 ? H : 1));
+    double *z = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    if (!hrow || !z) {
+        free(hrow);
+        free(z);
+        return -1;
+    }
+    for (int64_t i = 0; i < n_rows; ++i) {
+        logits_of_row(h, h_kind, rows[i], W, w_kind, H, V, hrow, z);
+        int64_t best = 0;
+        for (int64_t v = 1; v < V; ++v)
+            if (z[v] > z[best])
+                best = v;
+        const double l = log_sum_exp(z, V);
+        token[i] = best;
+        logp[i] = z[best] - l;
+        if (zmax)
+            zmax[i] = z[best];
+    }
+    free(hrow);
+    free(z);
+    return 0;
+}
