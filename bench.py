@@ -234,6 +234,75 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def time_loop(fn, reps: int, stream) -> float:
+    """Mean ms per call of `fn` over `reps` calls after 3 warm-up calls."""
+    import torch
+    for _ in range(3):
+        fn(0)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(reps):
+        fn(i)
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def measure_rows(rk, pool, zs, peaks, dev, stream) -> dict:
+    """The widened rows, each in its own loop on the GRPO / logits inputs."""
+    import torch
+    T, H, V = pool.h.shape[0], pool.H, pool.V
+    Tl, Vl = LOGITS["T"], LOGITS["V"]
+    h, W, tg = pool.h.to(dev), pool.W.to(dev), pool.targets.to(dev)
+    out = {}
+    # dense path lm_head on a 8192-row slice of the group (bf16 logits 2.1 GB)
+    Td = 8192
+    logits = torch.empty((Td, V), dtype=torch.bfloat16, device=dev)
+    ms = time_loop(lambda i: rk.lm_head(h[:Td], W, out=logits, stream=stream), 5, stream)
+    tf = 2.0 * Td * H * V / (ms / 1e3) / 1e12
+    out["lm_head"] = {"shape": [Td, H, V], "ms_per_call": ms, "bound": "tensor", "achieved": tf,
+                      "unit": "TFLOP/s", "peak": peaks["bf16_tflops"],
+                      "frac": tf / peaks["bf16_tflops"], "peak_source": "burst bf16"}
+    # logits-path backward (read bf16 logits, write fp32 dlogits), rotated inputs
+    g = torch.randn(Tl, device=dev)
+    lses = [rk.logp_from_logits(z, t, stream=stream)[1] for z, t in zs]
+    dl = torch.empty((Tl, Vl), dtype=torch.float32, device=dev)
+
+    def lbwd(i):
+        z, t = zs[i % len(zs)]
+        rk.logp_from_logits_bwd(z, t, lses[i % len(zs)], g, out=dl, stream=stream)
+    ms = time_loop(lbwd, 40, stream)
+    nbytes = Tl * Vl * 2 + Tl * Vl * 4 + Tl * 16
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out["logits_bwd"] = {"shape": [Tl, Vl], "ms_per_call": ms, "bound": "hbm", "achieved": gbs,
+                         "unit": "GB/s", "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+                         "bytes_per_call": nbytes}
+    # per-token GRPO loss on the group's rows
+    lp = torch.randn(T, device=dev) - 3
+    lpo = lp + 0.1 * torch.randn(T, device=dev)
+    lpr = lp + 0.1 * torch.randn(T, device=dev)
+    adv = torch.randn(T, device=dev)
+    ms = time_loop(lambda i: rk.grpo_token_loss(lp, lpo, adv, tg, logp_ref=lpr, beta=0.04,
+                                                stream=stream), 40, stream)
+    nbytes = T * (4 * 4 + 8 + 4 * 4)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out["grpo_token_loss"] = {"T": T, "ms_per_call": ms, "bound": "hbm", "achieved": gbs,
+                              "unit": "GB/s", "peak": peaks["hbm_gbs"],
+                              "frac": gbs / peaks["hbm_gbs"], "bytes_per_call": nbytes,
+                              "note": "0.4 MB per call: launch-latency bound"}
+    # fused greedy step on the whole group
+    wsg = torch.empty(rk.linear_greedy_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
+    ms = time_loop(lambda i: rk.linear_greedy(h, W, workspace=wsg, stream=stream), 3, stream)
+    tf = 2.0 * T * H * V / (ms / 1e3) / 1e12
+    out["linear_greedy"] = {"shape": [T, H, V], "ms_per_call": ms, "bound": "tensor",
+                            "achieved": tf, "unit": "TFLOP/s",
+                            "peak": peaks["bf16_tflops_sustained"],
+                            "frac": tf / peaks["bf16_tflops_sustained"]}
+    del logits, dl, wsg
+    return out
+
+
 def run_gpu(args) -> None:
     import torch
 
@@ -436,6 +505,10 @@ def run_gpu(args) -> None:
     if TRAFFIC_RECORD["source_sha1"] == kernel_source_sha1():
         traffic = TRAFFIC_RECORD["fwd_tiles_bytes"]
 
+    rows = None
+    if not args.no_rows:
+        rows = measure_rows(rk, pool, zs, peaks, dev, stream)
+
     cpu = None
     if not args.no_cpu_baseline:
         v, cores, desc = cpu_oracle_sample(pool, logits_host, args.cpu_rows)
@@ -470,6 +543,7 @@ def run_gpu(args) -> None:
                                     "frac": lg_gbs_step / peaks["hbm_gbs"],
                                     "note": "measured right after the dh GEMM: its dirty L2 "
                                             "lines are written back during this call"}},
+        "rows": rows,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
@@ -542,6 +616,8 @@ def main() -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rows", action="store_true",
+                    help="skip the separate timing of the widened rows")
     ap.add_argument("--case", choices=["fwd", "bwd", "logits"], default=None)
     ap.add_argument("--shape", default="2048,4096,32000")
     ap.add_argument("--reps", type=int, default=3)

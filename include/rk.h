@@ -143,6 +143,71 @@ rk_status rk_linear_logp_bwd(const uint16_t *h, const uint16_t *W, const int64_t
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The dense path's lm_head (chain index 6 of PR #264; "dense vs indexed
+ * selected-logprob paths", issue #101, Scope): logits[t, v] = bf16(sum_k
+ * h[t, k] * W[v, k]) with fp32 accumulation and one rounding to bf16, using the
+ * same tensor-core tiles as rk_linear_logp (one fixed tile shape and K order
+ * for every T, so a row's logits do not depend on the batch).
+ *   h bf16 [T, H], W bf16 [V, H] (16-byte aligned), logits bf16 [T, ld_logits]
+ *   (16-byte aligned, ld_logits >= V and a multiple of 8; columns >= V untouched).
+ * Supported: as rk_linear_logp.  Every row is computed (no mask).
+ */
+rk_status rk_lm_head(const uint16_t *h, const uint16_t *W, int64_t T, int64_t H, int64_t V,
+                     uint16_t *logits, int64_t ld_logits, void *stream);
+
+/*
+ * Logits-path backward (the gradient of the dense path, issue #244 Workstream
+ * 3: backward as a first-class property): for every active row,
+ *     dlogits[t, v] = g[t] * (onehot(targets[t])[v] - exp(logits[t, v] - lse[t]))
+ * in fp32 (0 on inactive rows; NaN and RK_DEVERR_TARGET_RANGE for targets >= V).
+ *   logits bf16 [T, V], lse fp32 [T] (from rk_logp_from_logits), grad_logp
+ *   fp32 [T], dlogits fp32 [T, V].  Each element is computed independently.
+ */
+rk_status rk_logp_from_logits_bwd(const uint16_t *logits, const int64_t *targets,
+                                  const int32_t *cu_seqlens, int32_t num_seqs,
+                                  int64_t T, int64_t V, const float *lse,
+                                  const float *grad_logp, float *dlogits, void *stream);
+
+/*
+ * Per-token GRPO loss on selected logprobs ("grpo_loss, ratio_kl", issue #101
+ * P0 list; chain index 9 of PR #264, whose review asks for per-token outputs
+ * or a fixed normalisation before bitwise invariance can be required; this
+ * operator is per token, with a caller-given `scale` standing for the
+ * caller's fixed denominator).  For every active row t:
+ *     ratio = exp(logp - logp_old)
+ *     surr  = min(ratio * A, clip(ratio, 1 - eps_low, 1 + eps_high) * A)
+ *     kl    = exp(logp_ref - logp) - (logp_ref - logp) - 1   (0 if logp_ref is NULL)
+ *     loss  = scale * (-surr + beta * kl)
+ *     grad_logp = d loss / d logp   (the g for rk_linear_logp_bwd)
+ * Inactive rows get 0 in every output.  All arrays fp32 [T]; logp_ref, ratio
+ * and kl may be NULL.  Requires 0 <= eps_low < 1, eps_high >= 0, beta >= 0.
+ */
+rk_status rk_grpo_token_loss(const float *logp, const float *logp_old, const float *logp_ref,
+                             const float *advantages, const int64_t *targets,
+                             const int32_t *cu_seqlens, int32_t num_seqs, int64_t T,
+                             float eps_low, float eps_high, float beta, float scale,
+                             float *loss, float *grad_logp, float *ratio, float *kl,
+                             void *stream);
+
+/*
+ * Greedy decoding step fused with its selected logprob: for every row (rows
+ * outside [cu_seqlens[0], cu_seqlens[num_seqs]) when cu_seqlens is given get
+ * token -1 and logp = lse = 0),
+ *     token[t] = argmax_v z[t, v]   (z = h . W^T; the lowest v among equal maxima)
+ *     logp[t]  = z[t, token[t]] - logsumexp_v z[t, v]
+ * with exactly the arithmetic of rk_linear_logp, so that scoring the generated
+ * tokens again later (rk_linear_logp with targets = token) reproduces logp and
+ * lse bit for bit (issue #244, Workstream 2 #152: generate-then-re-score
+ * selected-logprob equivalence).
+ *   workspace >= rk_linear_greedy_workspace_size(T, H, V) bytes, 16-byte aligned.
+ */
+size_t rk_linear_greedy_workspace_size(int64_t T, int64_t H, int64_t V);
+rk_status rk_linear_greedy(const uint16_t *h, const uint16_t *W, const int32_t *cu_seqlens,
+                           int32_t num_seqs, int64_t T, int64_t H, int64_t V,
+                           int64_t *token, float *logp, float *lse,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * rk_linear_logp without a workspace argument, for callers that cannot
  * allocate device memory.  (No counterpart in the pages: this is an interface
  * convenience, not part of the method.)  Such callers include programs whose

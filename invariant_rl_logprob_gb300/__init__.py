@@ -27,6 +27,8 @@ __all__ = [
     "linear_logp", "linear_logp_workspace_size",
     "logp_from_logits",
     "linear_logp_bwd", "linear_logp_bwd_workspace_size", "linear_logp_bwd_min_workspace_size",
+    "lm_head", "logp_from_logits_bwd", "grpo_token_loss", "linear_greedy",
+    "linear_greedy_workspace_size",
     "get_device_error", "selftest_wait_timeout", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT",
 ]
 
@@ -77,6 +79,18 @@ def load_library() -> ctypes.CDLL:
     lib.rk_linear_logp_bwd_min_workspace_size.restype = sz
     lib.rk_linear_logp_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, sz, vp]
     lib.rk_linear_logp_bwd.restype = ctypes.c_int
+    lib.rk_lm_head.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp]
+    lib.rk_lm_head.restype = ctypes.c_int
+    lib.rk_logp_from_logits_bwd.argtypes = [vp, vp, vp, i32, i64, i64, vp, vp, vp, vp]
+    lib.rk_logp_from_logits_bwd.restype = ctypes.c_int
+    f32 = ctypes.c_float
+    lib.rk_grpo_token_loss.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, f32, f32, f32, f32,
+                                       vp, vp, vp, vp, vp]
+    lib.rk_grpo_token_loss.restype = ctypes.c_int
+    lib.rk_linear_greedy_workspace_size.argtypes = [i64, i64, i64]
+    lib.rk_linear_greedy_workspace_size.restype = sz
+    lib.rk_linear_greedy.argtypes = [vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, sz, vp]
+    lib.rk_linear_greedy.restype = ctypes.c_int
     lib.rk_selftest_wait_timeout.argtypes = [i64, vp]
     lib.rk_selftest_wait_timeout.restype = ctypes.c_int
     lib.rk_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
@@ -213,6 +227,105 @@ def linear_logp_bwd(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, lse
                                 workspace.numel(), _stream_handle(stream, h.device))
     _check(st, "rk_linear_logp_bwd")
     return dh
+
+
+def lm_head(h: torch.Tensor, W: torch.Tensor, *, out: torch.Tensor | None = None,
+            stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Dense path: bf16 logits ``[T, V]`` = bf16(h W^T) (fp32 accumulation)."""
+    lib = load_library()
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    T, H = h.shape
+    V = W.shape[0]
+    if W.shape[1] != H or W.device != h.device:
+        raise ValueError("W must be [V, H] on h's device")
+    ld = (V + 7) // 8 * 8
+    if out is None:
+        buf = torch.empty((T, ld), dtype=torch.bfloat16, device=h.device)
+        out = buf[:, :V]
+    else:
+        if out.dtype != torch.bfloat16 or out.dim() != 2 or out.stride(1) != 1:
+            raise ValueError("out must be a bf16 [T, V] view with unit column stride")
+        ld = out.stride(0)
+    st = lib.rk_lm_head(_ptr(h), _ptr(W), T, H, V, _ptr(out), ld, _stream_handle(stream, h.device))
+    _check(st, "rk_lm_head")
+    return out
+
+
+def logp_from_logits_bwd(logits: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
+                         grad_logp: torch.Tensor, cu_seqlens: torch.Tensor | None = None, *,
+                         out: torch.Tensor | None = None,
+                         stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """dlogits = g (onehot - softmax(logits)) in fp32 ``[T, V]``."""
+    lib = load_library()
+    _need(logits, "logits", torch.bfloat16, 2)
+    T, V = logits.shape
+    cu, ns = _rows(targets, cu_seqlens, T, logits.device)
+    _need(lse, "lse", torch.float32, 1)
+    _need(grad_logp, "grad_logp", torch.float32, 1)
+    if out is None:
+        out = torch.empty((T, V), dtype=torch.float32, device=logits.device)
+    st = lib.rk_logp_from_logits_bwd(_ptr(logits), _ptr(targets), _ptr(cu), ns, T, V, _ptr(lse),
+                                     _ptr(grad_logp), _ptr(out),
+                                     _stream_handle(stream, logits.device))
+    _check(st, "rk_logp_from_logits_bwd")
+    return out
+
+
+def grpo_token_loss(logp: torch.Tensor, logp_old: torch.Tensor, advantages: torch.Tensor,
+                    targets: torch.Tensor, cu_seqlens: torch.Tensor | None = None, *,
+                    logp_ref: torch.Tensor | None = None, eps_low: float = 0.2,
+                    eps_high: float = 0.2, beta: float = 0.0, scale: float = 1.0,
+                    stream: torch.cuda.Stream | None = None) -> dict:
+    """Per-token GRPO loss: dict with fp32 ``loss``, ``grad`` (d loss/d logp),
+    ``ratio`` and ``kl``, each ``[T]``."""
+    lib = load_library()
+    for name, t in (("logp", logp), ("logp_old", logp_old), ("advantages", advantages)):
+        _need(t, name, torch.float32, 1)
+    T = logp.shape[0]
+    if logp_ref is not None:
+        _need(logp_ref, "logp_ref", torch.float32, 1)
+    cu, ns = _rows(targets, cu_seqlens, T, logp.device)
+    out = {k: torch.empty(T, dtype=torch.float32, device=logp.device)
+           for k in ("loss", "grad", "ratio", "kl")}
+    st = lib.rk_grpo_token_loss(_ptr(logp), _ptr(logp_old), _ptr(logp_ref), _ptr(advantages),
+                                _ptr(targets), _ptr(cu), ns, T, eps_low, eps_high, beta, scale,
+                                _ptr(out["loss"]), _ptr(out["grad"]), _ptr(out["ratio"]),
+                                _ptr(out["kl"]), _stream_handle(stream, logp.device))
+    _check(st, "rk_grpo_token_loss")
+    return out
+
+
+def linear_greedy_workspace_size(T: int, H: int, V: int) -> int:
+    return int(load_library().rk_linear_greedy_workspace_size(T, H, V))
+
+
+def linear_greedy(h: torch.Tensor, W: torch.Tensor, cu_seqlens: torch.Tensor | None = None, *,
+                  workspace: torch.Tensor | None = None,
+                  stream: torch.cuda.Stream | None = None):
+    """Greedy step: ``(token int64 [T], logp fp32 [T], lse fp32 [T])``."""
+    lib = load_library()
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    T, H = h.shape
+    V = W.shape[0]
+    if W.shape[1] != H or W.device != h.device:
+        raise ValueError("W must be [V, H] on h's device")
+    cu, ns = (None, 0)
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+        cu, ns = cu_seqlens, cu_seqlens.numel() - 1
+    token = torch.empty(T, dtype=torch.int64, device=h.device)
+    logp = torch.empty(T, dtype=torch.float32, device=h.device)
+    lse = torch.empty(T, dtype=torch.float32, device=h.device)
+    if workspace is None:
+        need = int(lib.rk_linear_greedy_workspace_size(T, H, V))
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
+    st = lib.rk_linear_greedy(_ptr(h), _ptr(W), _ptr(cu), ns, T, H, V, _ptr(token), _ptr(logp),
+                              _ptr(lse), _ptr(workspace), workspace.numel(),
+                              _stream_handle(stream, h.device))
+    _check(st, "rk_linear_greedy")
+    return token, logp, lse
 
 
 def selftest_wait_timeout(limit_ns: int, stream: torch.cuda.Stream | None = None) -> None:

@@ -31,7 +31,9 @@
 //         m = max z, s = sum 2^((z - m) log2 e), and z[target] if the target
 //         is in the tile, written to workspace[row][tile];
 //   kDz   dZ = g exp(z - lse) rounded to bf16 (0 on inactive rows);
-//   kDh   dh = g W[target] - acc in fp32 (0 on inactive rows).
+//   kDh   dh = g W[target] - acc in fp32 (0 on inactive rows);
+//   kLogits  z rounded to bf16 (the dense path's lm_head);
+//   kGreedy  kFwd plus the lowest column holding the tile maximum.
 // A second small kernel (linear_logp_merge) folds the forward partials of a
 // row in a fixed order into lse and logp.
 //
@@ -66,7 +68,10 @@ constexpr int kThreads = kEpiThreads + 64;
 constexpr int kGroupN = 16;  // raster group (in N tiles) of the forward / dZ GEMMs
 constexpr int kGroupNDh = 16;  // raster group (in H tiles) of the dh GEMM
 
-enum Mode { kFwd = 0, kDz = 1, kDh = 2 };
+// kFwd: forward partials; kDz: backward GEMM 1; kDh: backward GEMM 2;
+// kLogits: the dense path's lm_head (z stored as bf16); kGreedy: kFwd plus
+// each tile's argmax column (greedy decoding).
+enum Mode { kFwd = 0, kDz = 1, kDh = 2, kLogits = 3, kGreedy = 4 };
 
 // full / tmem_empty / drain are used in the even CTA only; empty and
 // tmem_full in both (the MMA commits are multicast to the pair).
@@ -95,6 +100,7 @@ struct TileArgs {
     // kFwd
     float2 *part;  // [rows][num_n]
     float *ztgt;   // [rows]
+    int32_t *pidx; // kGreedy: [rows][num_n] column of each tile's maximum
     // kDz
     const float *lse;   // [T] (global)
     const float *grad;  // [T] (global)
@@ -312,23 +318,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int64_t lrow = (int64_t)mb * 2 * BM + (int64_t)rank * BM + threadIdx.x;  // local row
             const bool in_range = lrow < a.rows;
             const int64_t grow = a.row0 + lrow;                    // global row
-            const int64_t tgt = in_range ? a.targets[grow] : -1;
+            const int64_t tgt = (in_range && a.targets != nullptr) ? a.targets[grow] : -1;
             const int n0 = nb * BN;
             const uint32_t empty_bar = mapa_shared(smem_u32(&ctl->tmem_empty[b]), 0);
-            if constexpr (MODE == kFwd) {
+            if constexpr (MODE == kFwd || MODE == kGreedy) {
                 const int valid = min(BN, a.V - n0);
                 const int tcol = (tgt >= n0 && tgt < (int64_t)n0 + valid) ? (int)(tgt - n0) : -1;
                 if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
                 tc_fence_after();
                 const uint32_t taddr = tmem + lane_off + (uint32_t)(b * BN);
-                // pass 1: the row's maximum over the tile
+                // pass 1: the row's maximum over the tile (and, greedy, its
+                // lowest column: a later column replaces it only if strictly larger)
                 float m = -INFINITY;
+                int arg = 0;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
                     tmem_ld_wait();
-                    if (valid == BN) {
+                    if constexpr (MODE == kGreedy) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float x = __uint_as_float(r[j]);
+                            if (c * 32 + j < valid && x > m) {
+                                m = x;
+                                arg = c * 32 + j;
+                            }
+                        }
+                    } else if (valid == BN) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) m = fmaxf(m, __uint_as_float(r[j]));
                     } else {
@@ -379,11 +396,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (in_range) {
                     a.part[lrow * a.num_n + nb] = make_float2(m, s);
                     if (tcol >= 0) a.ztgt[lrow] = zt;
+                    if constexpr (MODE == kGreedy) a.pidx[lrow * a.num_n + nb] = n0 + arg;
                 }
-            } else if constexpr (MODE == kDz) {
-                const bool active = in_range && row_active(grow, tgt, a.cu, a.num_seqs);
-                const float g = active ? a.grad[grow] : 0.f;
-                const float nl = active ? __fmul_rn(-a.lse[grow], kLog2e) : 0.f;
+            } else if constexpr (MODE == kDz || MODE == kLogits) {
+                constexpr bool kSoft = (MODE == kDz);
+                const bool active =
+                    in_range && (!kSoft || row_active(grow, tgt, a.cu, a.num_seqs));
+                const float g = (kSoft && active) ? a.grad[grow] : 0.f;
+                const float nl = (kSoft && active) ? __fmul_rn(-a.lse[grow], kLog2e) : 0.f;
                 const int valid = min(BN, a.V - n0);
                 if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
                 tc_fence_after();
@@ -397,10 +417,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     uint32_t pk[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float p0 = ex2(__fmaf_rn(__uint_as_float(r[2 * j]), kLog2e, nl));
-                        const float p1 = ex2(__fmaf_rn(__uint_as_float(r[2 * j + 1]), kLog2e, nl));
-                        const float d0 = active ? __fmul_rn(g, p0) : 0.f;
-                        const float d1 = active ? __fmul_rn(g, p1) : 0.f;
+                        float d0, d1;
+                        if constexpr (kSoft) {
+                            const float p0 = ex2(__fmaf_rn(__uint_as_float(r[2 * j]), kLog2e, nl));
+                            const float p1 =
+                                ex2(__fmaf_rn(__uint_as_float(r[2 * j + 1]), kLog2e, nl));
+                            d0 = active ? __fmul_rn(g, p0) : 0.f;
+                            d1 = active ? __fmul_rn(g, p1) : 0.f;
+                        } else {
+                            d0 = __uint_as_float(r[2 * j]);
+                            d1 = __uint_as_float(r[2 * j + 1]);
+                        }
                         pk[j] = pack_bf16x2(d0, d1);
                     }
                     if (in_range) {
@@ -485,6 +512,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 constexpr int kMergeRowsPerBlock = 8;
 
+// The row's log-sum-exp from its tile partials: lane l folds tiles l, l+32,
+// ... in ascending order, then a fixed xor tree; every lane ends with the
+// same (m, s).  Shared by the forward and greedy merges, so a greedy step and
+// a later scoring of its token give the same lse bit for bit.
+__device__ __forceinline__ void fold_tiles(const float2 *__restrict__ pr, int num_n, int lane,
+                                           float &m, float &s) {
+    m = -INFINITY;
+    s = 0.f;
+#pragma unroll 4
+    for (int j = lane; j < num_n; j += 32) {
+        const float2 p = pr[j];
+        lse_merge(m, s, p.x, p.y);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+        const float so = __shfl_xor_sync(0xffffffffu, s, off);
+        lse_merge(m, s, mo, so);
+    }
+}
+
 __global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
     linear_logp_merge(const float2 *__restrict__ part, const float *__restrict__ ztgt,
                       const int64_t *__restrict__ targets, const int32_t *__restrict__ cu,
@@ -509,22 +557,59 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
         }
         return;
     }
-    const float2 *pr = part + row * num_n;
-    float m = -INFINITY, s = 0.f;
-#pragma unroll 4
-    for (int j = lane; j < num_n; j += 32) {
-        const float2 p = pr[j];
-        lse_merge(m, s, p.x, p.y);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-        const float so = __shfl_xor_sync(0xffffffffu, s, off);
-        lse_merge(m, s, mo, so);
-    }
+    float m, s;
+    fold_tiles(part + row * num_n, num_n, lane, m, s);
     if (lane == 0) {
         const float l = __fadd_rn(m, logf(s));
         logp[row] = __fsub_rn(ztgt[row], l);
+        if (lse) lse[row] = l;
+    }
+}
+
+// Greedy step: the token with the largest logit (lowest index among equal
+// maxima; ties across tiles resolve to the lower tile) and its logprob.
+__global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
+    linear_greedy_merge(const float2 *__restrict__ part, const int32_t *__restrict__ pidx,
+                        const int32_t *__restrict__ cu, int num_seqs, int64_t T, int32_t num_n,
+                        int64_t *__restrict__ token, float *__restrict__ logp,
+                        float *__restrict__ lse) {
+    const int64_t row = (int64_t)blockIdx.x * kMergeRowsPerBlock + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= T) return;
+    const bool active = cu == nullptr || (row >= (int64_t)cu[0] && row < (int64_t)cu[num_seqs]);
+    if (!active) {
+        if (lane == 0) {
+            token[row] = -1;
+            logp[row] = 0.f;
+            if (lse) lse[row] = 0.f;
+        }
+        return;
+    }
+    float m, s;
+    fold_tiles(part + row * num_n, num_n, lane, m, s);
+    float bm = -INFINITY;
+    int32_t bi = 0x7fffffff;
+    for (int j = lane; j < num_n; j += 32) {
+        const float x = part[row * num_n + j].x;
+        const int32_t i = pidx[row * num_n + j];
+        if (x > bm || (x == bm && i < bi)) {
+            bm = x;
+            bi = i;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float xo = __shfl_xor_sync(0xffffffffu, bm, off);
+        const int32_t io = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (xo > bm || (xo == bm && io < bi)) {
+            bm = xo;
+            bi = io;
+        }
+    }
+    if (lane == 0) {
+        const float l = __fadd_rn(m, logf(s));
+        token[row] = bi;
+        logp[row] = __fsub_rn(bm, l);
         if (lse) lse[row] = l;
     }
 }
@@ -631,6 +716,70 @@ cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_
                                                                   num_seqs, T, a.V, a.num_n, logp,
                                                                   lse, di.err);
     return cudaGetLastError();
+}
+
+size_t linear_greedy_workspace_bytes(int64_t T, int64_t V) {
+    if (T <= 0) return 0;
+    const int64_t num_n = (V + BN - 1) / BN;
+    return linear_fwd_workspace_bytes(T, V) + round256((size_t)T * (size_t)num_n * sizeof(int32_t));
+}
+
+cudaError_t launch_linear_greedy(const uint16_t *h, const uint16_t *W, const int32_t *cu,
+                                 int num_seqs, int64_t T, int64_t H, int64_t V, int64_t *token,
+                                 float *logp, float *lse, void *workspace, const DeviceInfo &di,
+                                 cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    CUtensorMap tmA, tmB;
+    if (!encode_tmap_bf16_2d(&tmA, h, (uint64_t)H, (uint64_t)T, (uint64_t)H * 2, BK, BM, true))
+        return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16_2d(&tmB, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2, true))
+        return cudaErrorInvalidValue;
+    TileArgs a{};
+    a.targets = nullptr;
+    a.cu = cu;
+    a.num_seqs = num_seqs;
+    a.row0 = 0;
+    a.rows = T;
+    a.V = (int32_t)V;
+    a.H = (int32_t)H;
+    a.num_m = (int32_t)((T + 2 * BM - 1) / (2 * BM));
+    a.num_n = (int32_t)((V + BN - 1) / BN);
+    a.num_k = (int32_t)(H / BK);
+    a.err = di.err;
+    uint8_t *w = reinterpret_cast<uint8_t *>(workspace);
+    a.part = reinterpret_cast<float2 *>(w);
+    const size_t fwd_bytes = linear_fwd_workspace_bytes(T, V);
+    a.ztgt = reinterpret_cast<float *>(w + round256((size_t)T * (size_t)a.num_n * sizeof(float2)));
+    a.pidx = reinterpret_cast<int32_t *>(w + fwd_bytes);
+    cudaError_t e = run_tiles<kGreedy>(tmA, tmB, a, di, st);
+    if (e != cudaSuccess) return e;
+    const unsigned mgrid = (unsigned)((T + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock);
+    linear_greedy_merge<<<mgrid, 32 * kMergeRowsPerBlock, 0, st>>>(a.part, a.pidx, cu, num_seqs, T,
+                                                                    a.num_n, token, logp, lse);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lm_head(const uint16_t *h, const uint16_t *W, int64_t T, int64_t H, int64_t V,
+                           uint16_t *logits, int64_t ld, const DeviceInfo &di, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    CUtensorMap tmA, tmB;
+    if (!encode_tmap_bf16_2d(&tmA, h, (uint64_t)H, (uint64_t)T, (uint64_t)H * 2, BK, BM, true))
+        return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16_2d(&tmB, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2, true))
+        return cudaErrorInvalidValue;
+    TileArgs a{};
+    a.targets = nullptr;
+    a.row0 = 0;
+    a.rows = T;
+    a.V = (int32_t)V;
+    a.H = (int32_t)H;
+    a.num_m = (int32_t)((T + 2 * BM - 1) / (2 * BM));
+    a.num_n = (int32_t)((V + BN - 1) / BN);
+    a.num_k = (int32_t)(H / BK);
+    a.err = di.err;
+    a.dz = logits;
+    a.ldz = ld;
+    return run_tiles<kLogits>(tmA, tmB, a, di, st);
 }
 
 int64_t linear_bwd_chunk_quantum() { return BM; }

@@ -163,7 +163,89 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Logits-path backward: dlogits[t, v] = g[t] * (onehot(target_t)[v] - p[t, v]),
+// p = 2^((z - lse) log2 e), written in fp32; each element is independent, so
+// the result of a row depends only on that row, its lse and its g.  Two warps
+// per row; virtual lane vl owns groups vl, vl + 64, ... of 8 columns.
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads)
+    logits_bwd_kernel(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targets,
+                      const int32_t *__restrict__ cu, int num_seqs, int64_t T, int64_t V,
+                      const float *__restrict__ lse, const float *__restrict__ grad,
+                      float *__restrict__ dlogits, unsigned *err) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int vl = (warp % kWarpsPerRow) * 32 + lane;
+    const int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + warp / kWarpsPerRow;
+    if (row >= T) return;
+    const int64_t tgt = targets[row];
+    const bool active = row_active(row, tgt, cu, num_seqs);
+    const bool bad = active && tgt >= V;
+    if (bad && vl == 0) atomicOr(err, kErrTargetRange);
+    const bool live = active && !bad;
+    const float g = live ? grad[row] : 0.f;
+    const float nl = live ? __fmul_rn(-lse[row], kLog2e) : 0.f;
+    const float fill = bad ? __int_as_float(0x7fc00000) : 0.f;
+    const uint16_t *zrow = logits + row * V;
+    float *orow = dlogits + row * V;
+    const int64_t G = (V + 7) >> 3;
+#pragma unroll 4
+    for (int64_t gi = vl; gi < G; gi += kLanesPerRow) {
+        const int64_t c0 = gi << 3;
+        float z[8];
+        if (VEC) {
+            const uint4 w = live ? ld_stream_v4(reinterpret_cast<const uint4 *>(zrow) + gi)
+                                 : make_uint4(0, 0, 0, 0);
+            z[0] = bf16_lo(w.x);
+            z[1] = bf16_hi(w.x);
+            z[2] = bf16_lo(w.y);
+            z[3] = bf16_hi(w.y);
+            z[4] = bf16_lo(w.z);
+            z[5] = bf16_hi(w.z);
+            z[6] = bf16_lo(w.w);
+            z[7] = bf16_hi(w.w);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                z[j] = (live && c0 + j < V) ? bf16_bits_to_f32(__ldg(zrow + c0 + j)) : 0.f;
+        }
+        float d[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float p = ex2(__fmaf_rn(z[j], kLog2e, nl));
+            const float oh = (c0 + j == tgt) ? 1.f : 0.f;
+            d[j] = live ? __fmul_rn(g, __fsub_rn(oh, p)) : fill;
+        }
+        if (VEC) {
+            float4 *dst = reinterpret_cast<float4 *>(orow + c0);
+            dst[0] = make_float4(d[0], d[1], d[2], d[3]);
+            dst[1] = make_float4(d[4], d[5], d[6], d[7]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (c0 + j < V) orow[c0 + j] = d[j];
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_logits_bwd(const uint16_t *logits, const int64_t *targets, const int32_t *cu,
+                              int num_seqs, int64_t T, int64_t V, const float *lse,
+                              const float *grad, float *dlogits, const DeviceInfo &di,
+                              cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)((T + kRowsPerBlock - 1) / kRowsPerBlock);
+    const bool vec = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(dlogits) & 15u) == 0);
+    if (vec)
+        logits_bwd_kernel<true><<<grid, kThreads, 0, st>>>(logits, targets, cu, num_seqs, T, V,
+                                                           lse, grad, dlogits, di.err);
+    else
+        logits_bwd_kernel<false><<<grid, kThreads, 0, st>>>(logits, targets, cu, num_seqs, T, V,
+                                                            lse, grad, dlogits, di.err);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_logits_logp(const uint16_t *logits, const int64_t *targets, const int32_t *cu,
                                int num_seqs, int64_t T, int64_t V, float *logp, float *lse,

@@ -235,6 +235,94 @@ rk_status rk_linear_logp_bwd(const uint16_t *h, const uint16_t *W, const int64_t
     return RK_OK;
 }
 
+rk_status rk_lm_head(const uint16_t *h, const uint16_t *W, int64_t T, int64_t H, int64_t V,
+                     uint16_t *logits, int64_t ld_logits, void *stream) {
+    if (T < 0 || H <= 0 || V <= 0) return RK_ERR_INVALID_ARG;
+    if (T == 0) return RK_OK;
+    if (!h || !W || !logits || ld_logits < V) return RK_ERR_INVALID_ARG;
+    if (H % 64 != 0 || H > 65536 || V >= (int64_t(1) << 31) || T >= (int64_t(1) << 31))
+        return RK_ERR_UNSUPPORTED;
+    if (!aligned(h, 16) || !aligned(W, 16) || !aligned(logits, 16) || ld_logits % 8 != 0)
+        return RK_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    e = rk::launch_lm_head(h, W, T, H, V, logits, ld_logits, di, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    return RK_OK;
+}
+
+rk_status rk_logp_from_logits_bwd(const uint16_t *logits, const int64_t *targets,
+                                  const int32_t *cu_seqlens, int32_t num_seqs, int64_t T,
+                                  int64_t V, const float *lse, const float *grad_logp,
+                                  float *dlogits, void *stream) {
+    if (T < 0 || V <= 0) return RK_ERR_INVALID_ARG;
+    if (T == 0) return RK_OK;
+    if (!logits || !lse || !grad_logp || !dlogits) return RK_ERR_INVALID_ARG;
+    rk_status st = check_rows(targets, cu_seqlens, num_seqs);
+    if (st != RK_OK) return st;
+    if (V >= (int64_t(1) << 31)) return RK_ERR_UNSUPPORTED;
+    if (!aligned(logits, 2) || !aligned(dlogits, 4)) return RK_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    e = rk::launch_logits_bwd(logits, targets, cu_seqlens, num_seqs, T, V, lse, grad_logp, dlogits,
+                              di, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    return RK_OK;
+}
+
+rk_status rk_grpo_token_loss(const float *logp, const float *logp_old, const float *logp_ref,
+                             const float *advantages, const int64_t *targets,
+                             const int32_t *cu_seqlens, int32_t num_seqs, int64_t T,
+                             float eps_low, float eps_high, float beta, float scale, float *loss,
+                             float *grad_logp, float *ratio, float *kl, void *stream) {
+    if (T < 0) return RK_ERR_INVALID_ARG;
+    if (T == 0) return RK_OK;
+    if (!logp || !logp_old || !advantages || !loss || !grad_logp) return RK_ERR_INVALID_ARG;
+    rk_status st = check_rows(targets, cu_seqlens, num_seqs);
+    if (st != RK_OK) return st;
+    if (!(eps_low >= 0.f && eps_low < 1.f) || !(eps_high >= 0.f) || !(beta >= 0.f))
+        return RK_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    e = rk::launch_grpo_token(logp, logp_old, logp_ref, advantages, targets, cu_seqlens, num_seqs,
+                              T, eps_low, eps_high, beta, scale, loss, grad_logp, ratio, kl, di,
+                              static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    return RK_OK;
+}
+
+size_t rk_linear_greedy_workspace_size(int64_t T, int64_t H, int64_t V) {
+    (void)H;
+    if (T <= 0 || V <= 0) return 0;
+    return rk::linear_greedy_workspace_bytes(T, V);
+}
+
+rk_status rk_linear_greedy(const uint16_t *h, const uint16_t *W, const int32_t *cu_seqlens,
+                           int32_t num_seqs, int64_t T, int64_t H, int64_t V, int64_t *token,
+                           float *logp, float *lse, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+    if (T < 0 || H <= 0 || V <= 0) return RK_ERR_INVALID_ARG;
+    if (T == 0) return RK_OK;
+    if (!h || !W || !token || !logp) return RK_ERR_INVALID_ARG;
+    if (cu_seqlens && num_seqs < 0) return RK_ERR_INVALID_ARG;
+    if (H % 64 != 0 || H > 65536 || V >= (int64_t(1) << 31) || T >= (int64_t(1) << 31))
+        return RK_ERR_UNSUPPORTED;
+    if (!aligned(h, 16) || !aligned(W, 16)) return RK_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < rk::linear_greedy_workspace_bytes(T, V))
+        return RK_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return RK_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    e = rk::launch_linear_greedy(h, W, cu_seqlens, num_seqs, T, H, V, token, logp, lse, workspace,
+                                 di, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    return RK_OK;
+}
+
 rk_status rk_selftest_wait_timeout(int64_t limit_ns, void *stream) {
     if (limit_ns <= 0 || limit_ns > 10000000000ll) return RK_ERR_INVALID_ARG;
     DeviceInfo di;

@@ -37,14 +37,36 @@ cudaError_t launch_logits_logp(const uint16_t *logits, const int64_t *targets, c
                                int num_seqs, int64_t T, int64_t V, float *logp, float *lse,
                                const DeviceInfo &di, cudaStream_t st);
 
-// ---- linear_logp forward (linear_logp_fwd.cu) ----
+// ---- linear_logp forward (linear_logp_tc.cu) ----
 size_t linear_fwd_workspace_bytes(int64_t T, int64_t V);
 cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
                               const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
                               float *logp, float *lse, void *workspace, const DeviceInfo &di,
                               cudaStream_t st);
 
-// ---- linear_logp backward (linear_logp_bwd.cu) ----
+// ---- greedy step and dense lm_head (linear_logp_tc.cu) ----
+size_t linear_greedy_workspace_bytes(int64_t T, int64_t V);
+cudaError_t launch_linear_greedy(const uint16_t *h, const uint16_t *W, const int32_t *cu,
+                                 int num_seqs, int64_t T, int64_t H, int64_t V, int64_t *token,
+                                 float *logp, float *lse, void *workspace, const DeviceInfo &di,
+                                 cudaStream_t st);
+cudaError_t launch_lm_head(const uint16_t *h, const uint16_t *W, int64_t T, int64_t H, int64_t V,
+                           uint16_t *logits, int64_t ld, const DeviceInfo &di, cudaStream_t st);
+
+// ---- logits-path backward (logits_logp.cu) ----
+cudaError_t launch_logits_bwd(const uint16_t *logits, const int64_t *targets, const int32_t *cu,
+                              int num_seqs, int64_t T, int64_t V, const float *lse,
+                              const float *grad, float *dlogits, const DeviceInfo &di,
+                              cudaStream_t st);
+
+// ---- per-token GRPO loss (token_loss.cu) ----
+cudaError_t launch_grpo_token(const float *logp, const float *logp_old, const float *logp_ref,
+                              const float *adv, const int64_t *targets, const int32_t *cu,
+                              int num_seqs, int64_t T, float eps_low, float eps_high, float beta,
+                              float scale, float *loss, float *grad, float *ratio, float *kl,
+                              const DeviceInfo &di, cudaStream_t st);
+
+// ---- linear_logp backward (linear_logp_tc.cu) ----
 size_t linear_bwd_chunk_bytes(int64_t rows, int64_t V);
 int64_t linear_bwd_chunk_quantum();
 cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
