@@ -45,10 +45,24 @@ N_LOGITS_BUFFERS = 4
 WORKLOAD = ("grpo_fwd_bwd: linear_logp fwd+bwd T=65536 (64x1024) H=4096 V=128256 bf16, "
             "+ logits path T=2048 V=32000 bf16")
 
-# ncu dram__bytes_read.sum + dram__bytes_write.sum of the tile kernel, per
-# launch, scaled to the full workload, recorded together with a hash of the
-# kernel source; reported only while the source still matches.
-TRAFFIC_RECORD = {"source_sha1": None, "fwd_tiles_bytes": None}
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of the three tile-kernel
+# launches of one step (forward, dZ GEMM, dh GEMM) on this very workload
+# (`ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
+#  --clock-control none -k regex:linear_logp_tiles -c 3 python bench.py --steps 3
+#  --warmup 3 --no-cpu-baseline --no-rows`, one pass per launch), recorded with
+# the SHA-1 of the kernel source; reported only while the source still matches.
+TRAFFIC_RECORD = {
+    "source_sha1": "3bf799eabbf16c340be346d2d94f5973e9857dcb",
+    "bytes_per_step": 465151402496,
+    "per_launch_gb": {"fwd": 153.75, "dZ": 90.30, "dh": 221.10},
+}
+# Unique bytes a step has to move: forward h + W + partials; dZ GEMM h + W +
+# dZ written; dh GEMM dZ + W read, dh written.
+def algorithmic_bytes_per_step(T: int, H: int, V: int) -> int:
+    nt = (V + 255) // 256
+    h, w = T * H * 2, V * H * 2
+    dz = T * V * 2
+    return (h + w + T * nt * 8 + T * 4) + (h + w + dz) + (dz + w + T * H * 4)
 
 
 def kernel_source_sha1() -> str:
@@ -234,13 +248,24 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def hold_stream(stream, ms: float = 5.0) -> None:
+    """Keep `stream` busy for about `ms` so that the launches queued after it
+    run back to back on the device, whatever the host's per-call overhead."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(ms * 2.1e6))
+
+
 def time_loop(fn, reps: int, stream) -> float:
-    """Mean ms per call of `fn` over `reps` calls after 3 warm-up calls."""
+    """Mean device ms per call of `fn` over `reps` back-to-back calls (after 3
+    warm-up calls; the calls are queued behind a device-side wait so that
+    host overhead cannot leave gaps between them)."""
     import torch
     for _ in range(3):
         fn(0)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
+    hold_stream(stream, 2.0 + 0.05 * reps)
     a.record(stream)
     for i in range(reps):
         fn(i)
@@ -290,7 +315,7 @@ def measure_rows(rk, pool, zs, peaks, dev, stream) -> dict:
     out["grpo_token_loss"] = {"T": T, "ms_per_call": ms, "bound": "hbm", "achieved": gbs,
                               "unit": "GB/s", "peak": peaks["hbm_gbs"],
                               "frac": gbs / peaks["hbm_gbs"], "bytes_per_call": nbytes,
-                              "note": "0.4 MB per call: launch-latency bound"}
+                              "note": "2.6 MB per call: launch-latency bound"}
     # fused greedy step on the whole group
     wsg = torch.empty(rk.linear_greedy_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
     ms = time_loop(lambda i: rk.linear_greedy(h, W, workspace=wsg, stream=stream), 3, stream)
@@ -393,6 +418,7 @@ def run_gpu(args) -> None:
         rk.logp_from_logits(z, zt, out=zlogp, lse=zlse, stream=stream)
     ls0 = torch.cuda.Event(enable_timing=True)
     ls1 = torch.cuda.Event(enable_timing=True)
+    hold_stream(stream, 5.0)
     ls0.record(stream)
     for i in range(lg_reps):
         z, zt = zs[i % len(zs)]
@@ -502,8 +528,8 @@ def run_gpu(args) -> None:
     lg_gbs = lg_bytes / (lg_loop_ms / 1000.0) / 1e9
     lg_gbs_step = lg_bytes / (lg_ms / 1000.0) / 1e9
     traffic = None
-    if TRAFFIC_RECORD["source_sha1"] == kernel_source_sha1():
-        traffic = TRAFFIC_RECORD["fwd_tiles_bytes"]
+    if TRAFFIC_RECORD["source_sha1"] == kernel_source_sha1() and (T, H, V) == (65536, 4096, 128256):
+        traffic = TRAFFIC_RECORD["bytes_per_step"]
 
     rows = None
     if not args.no_rows:
@@ -528,6 +554,9 @@ def run_gpu(args) -> None:
                      "kernel": "linear_logp_tiles (fwd + dZ + dh launches; each timed with the "
                                "small kernels of its call)",
                      "algorithmic": "6*T*H*V flop per step (2 fwd + 2 z-recompute + 2 dZ.W)",
+                     "traffic_unit": "DRAM bytes per step (3 tile launches, ncu)",
+                     "traffic_per_launch_gb": TRAFFIC_RECORD["per_launch_gb"] if traffic else None,
+                     "algorithmic_bytes": algorithmic_bytes_per_step(T, H, V),
                      "peak_source": f"{peaks['source']} bf16_tflops_sustained"},
         "components_ms": {"linear_logp_fwd": fwd_ms, "linear_logp_bwd": bwd_ms,
                           "logits_path": lg_ms},
@@ -537,8 +566,9 @@ def run_gpu(args) -> None:
                         "unit": "GB/s", "frac": lg_gbs / peaks["hbm_gbs"],
                         "bytes_per_call": lg_bytes, "us_per_call": lg_loop_ms * 1000.0,
                         "tokens_per_s": Tl / (lg_loop_ms / 1000.0),
-                        "timing": f"{lg_reps} calls over {N_LOGITS_BUFFERS} rotated buffers "
-                                  "after the step loop (CUDA events, launching stream)",
+                        "timing": f"{lg_reps} back-to-back calls over {N_LOGITS_BUFFERS} rotated "
+                                  "buffers after the step loop (CUDA events on the launching "
+                                  "stream; queued behind a device-side wait)",
                         "in_step": {"us_per_call": lg_ms * 1000.0, "achieved": lg_gbs_step,
                                     "frac": lg_gbs_step / peaks["hbm_gbs"],
                                     "note": "measured right after the dh GEMM: its dirty L2 "
