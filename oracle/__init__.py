@@ -75,6 +75,8 @@ def _load():
         lib.oracle_grpo_token.restype = None
         lib.oracle_linear_greedy.argtypes = [vp, i32, vp, i32, vp, i64, i64, i64, vp, vp, vp]
         lib.oracle_linear_greedy.restype = i32
+        lib.oracle_linear_logp_dw.argtypes = [vp, i32, vp, i32, vp, vp, vp, i64, i64, i64, vp]
+        lib.oracle_linear_logp_dw.restype = i32
         _lib = lib
     return _lib
 
@@ -256,6 +258,24 @@ def linear_greedy(h, W, rows=None):
                                                   H, V, _ptr(tok), _ptr(lp), _ptr(zm)) != 0:
         raise MemoryError("oracle_linear_greedy")
     return tok, lp, zm
+
+
+def linear_logp_dw(h, W, targets, grad_logp, cu_seqlens=None, rows=None) -> np.ndarray:
+    """dW [V, H] in float64 = sum over the active rows (in the given order) of
+    g (onehot - softmax(h W^T))^T h."""
+    h, hk = _as_matrix(h)
+    W, wk = _as_matrix(W)
+    targets = np.ascontiguousarray(targets, dtype=np.int64)
+    g = np.ascontiguousarray(grad_logp, dtype=np.float64)
+    T, H = h.shape
+    V = W.shape[0]
+    rows, act = _rows_to_run(targets, cu_seqlens, rows)
+    run = np.ascontiguousarray(rows[act])
+    dW = np.zeros((V, H), dtype=np.float64)
+    if run.size and _load().oracle_linear_logp_dw(_ptr(h), hk, _ptr(W), wk, _ptr(targets), _ptr(g),
+                                                  _ptr(run), run.size, H, V, _ptr(dW)) != 0:
+        raise ValueError("oracle_linear_logp_dw: target out of range or out of memory")
+    return dW
 
 
 def bf16_bits_to_f64(bits) -> np.ndarray:

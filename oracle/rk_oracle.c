@@ -351,3 +351,48 @@ int oracle_linear_greedy(const void *h, int h_kind, const void *W, int w_kind,
     free(z);
     return 0;
 }
+
+/*
+ * linear_logp backward with respect to W over the listed rows (dW, a
+ * parameter gradient: a sum over tokens, issue #244 "[WS1 Test] ...",
+ * Workstream 3 #153 -- "GEMM dW", fixed batch-shape-independent order, and
+ * "compare parameter gradients over the same complete logical sample set"):
+ *   dW[v, k] = sum_i g[r_i] * (onehot(target_{r_i})[v] - p_{r_i}[v]) * h[r_i, k]
+ * with p = softmax(h . W^T) recomputed here; rows are summed in the listed
+ * order.  dW: [V, H] (overwritten).
+ */
+int oracle_linear_logp_dw(const void *h, int h_kind, const void *W, int w_kind,
+                          const int64_t *targets, const double *grad_logp,
+                          const int64_t *rows, int64_t n_rows, int64_t H, int64_t V, double *dW)
+{
+    double *hrow = (double *)malloc(sizeof(double) * (size_t)(H > 0 ? H : 1));
+    double *z = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    if (!hrow || !z) {
+        free(hrow);
+        free(z);
+        return -1;
+    }
+    for (int64_t i = 0; i < V * H; ++i)
+        dW[i] = 0.0;
+    int rc = 0;
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const int64_t r = rows[i];
+        const int64_t t = targets[r];
+        if (t < 0 || t >= V) {
+            rc = -1;
+            break;
+        }
+        logits_of_row(h, h_kind, r, W, w_kind, H, V, hrow, z);
+        const double l = log_sum_exp(z, V);
+        const double g = grad_logp[r];
+        for (int64_t v = 0; v < V; ++v) {
+            const double c = g * ((v == t ? 1.0 : 0.0) - exp(z[v] - l));
+            double *out = dW + v * H;
+            for (int64_t k = 0; k < H; ++k)
+                out[k] += c * hrow[k];
+        }
+    }
+    free(hrow);
+    free(z);
+    return rc;
+}

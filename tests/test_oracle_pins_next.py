@@ -143,3 +143,53 @@ def test_greedy_ties_take_lowest_index(oracle_mod):
     tok, lp, _ = oracle_mod.linear_greedy(h, W)
     assert tok[0] == 3
     assert abs(lp[0] - (2.0 - math.log(2 * math.exp(2.0) + 8))) < 1e-12
+
+
+# ---- dW ----
+
+@pytest.mark.parametrize("H,V,T", [(16, 7, 5), (32, 40, 9)])
+def test_dw_vs_torch_autograd(oracle_mod, H, V, T):
+    g = synth.generator(400 + H + V)
+    W = synth.normal_bf16(g, (V, H), 0.5)
+    h = synth.normal_bf16(g, (T, H), 1.0)
+    tg = synth.uniform_targets(g, T, V)
+    gr = torch.randn(T, generator=g, dtype=torch.float64)
+    dW = oracle_mod.linear_logp_dw(synth.bf16_bits(h), synth.bf16_bits(W), tg.numpy(), gr.numpy())
+    WW = W.double().clone().requires_grad_(True)
+    ls = torch.log_softmax(h.double() @ WW.T, dim=1)
+    (ls[torch.arange(T), tg] * gr).sum().backward()
+    np.testing.assert_allclose(dW, WW.grad.numpy(), atol=1e-12, rtol=0)
+
+
+def test_dw_finite_differences_and_columns(oracle_mod):
+    rng = np.random.default_rng(21)
+    H, V, T = 6, 5, 4
+    W = rng.normal(0, 0.7, (V, H))
+    h = rng.normal(0, 1, (T, H))
+    tg = rng.integers(0, V, T)
+    gr = rng.normal(0, 1, T)
+    dW = oracle_mod.linear_logp_dw(h, W, tg, gr)
+    eps = 1e-6
+
+    def f(WW):
+        lp, _ = oracle_mod.linear_logp(h, WW, tg)
+        return float(np.dot(gr, lp))
+    for v in range(V):
+        for k in range(H):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[v, k] += eps
+            Wm[v, k] -= eps
+            assert abs((f(Wp) - f(Wm)) / (2 * eps) - dW[v, k]) < 1e-7
+    # sum over v of dW[v, :] = sum_t g_t (1 - 1) h_t = 0
+    np.testing.assert_allclose(dW.sum(axis=0), 0.0, atol=1e-12)
+
+
+def test_dw_masking(oracle_mod):
+    rng = np.random.default_rng(22)
+    W = rng.normal(0, 1, (5, 4))
+    h = rng.normal(0, 1, (3, 4))
+    full = oracle_mod.linear_logp_dw(h, W, np.array([1, 2, 3]), np.ones(3))
+    part = oracle_mod.linear_logp_dw(h, W, np.array([1, -100, 3]), np.ones(3))
+    only = oracle_mod.linear_logp_dw(h[[0, 2]], W, np.array([1, 3]), np.ones(2))
+    np.testing.assert_allclose(part, only, atol=1e-15)
+    assert not np.allclose(full, part)
