@@ -325,6 +325,21 @@ def measure_rows(rk, pool, zs, peaks, dev, stream) -> dict:
                             "peak": peaks["bf16_tflops_sustained"],
                             "frac": tf / peaks["bf16_tflops_sustained"]}
     del logits, dl, wsg
+    # weight gradient on the whole group: dZ recomputed over the canonical
+    # tokens + the dW GEMM (K = tokens), 4*T*H*V flop
+    g = torch.randn(T, device=dev)
+    _, lse = rk.linear_logp(h, W, tg, stream=stream)
+    wsd = torch.empty(rk.linear_logp_dw_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
+    dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    ms = time_loop(lambda i: rk.linear_logp_dw(h, W, tg, lse, g, dW=dW, workspace=wsd,
+                                               stream=stream), 3, stream)
+    tf = 4.0 * T * H * V / (ms / 1e3) / 1e12
+    out["linear_logp_dw"] = {"shape": [T, H, V], "ms_per_call": ms, "bound": "tensor",
+                             "achieved": tf, "unit": "TFLOP/s",
+                             "peak": peaks["bf16_tflops_sustained"],
+                             "frac": tf / peaks["bf16_tflops_sustained"],
+                             "algorithmic": "4*T*H*V flop (dZ recompute + dZ^T h)"}
+    del wsd, dW
     return out
 
 

@@ -208,6 +208,36 @@ rk_status rk_linear_greedy(const uint16_t *h, const uint16_t *W, const int32_t *
                            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Weight gradient of linear_logp (issue #244 "[WS1 Test] ...", Workstream 3
+ * #153: "GEMM dW", fixed batch-shape-independent reduction order, no
+ * atomicAdd; parameter gradients are compared "over the same complete
+ * logical sample set", with packed/chunked results restored to canonical
+ * (sample_id, token_position) order):
+ *     dW[v, :] = sum over canonical tokens i of g_i * (onehot(target_i)[v] - p_i[v]) * h_i
+ * with p_i = softmax(h_i . W^T) recomputed from lse.  The canonical tokens are
+ * the active rows among `row_order[0..n_order)` (physical row indices, in the
+ * caller's canonical order; out-of-range entries are skipped), or among rows
+ * 0..T-1 in ascending order when row_order is NULL.  The sum runs over the
+ * canonical tokens in that order: the same tokens in the same canonical
+ * order give a bitwise identical dW whatever their physical layout
+ * (padding, packing, permutation, batch composition).
+ *   h, W, targets, cu_seqlens, num_seqs, T, H, V: as for rk_linear_logp
+ *   lse, grad_logp fp32 [T]; dW fp32 [V, H] output (16-byte aligned);
+ *   workspace >= rk_linear_logp_dw_workspace_size(n, H, V) bytes, where n is
+ *   n_order (or T): canonical copies of h and of g * softmax (bf16 [n, V]).
+ * The one-hot term is accumulated in fp32 per vocabulary row over its
+ * tokens in canonical order; the softmax term is a tensor-core GEMM with
+ * K = the canonical tokens in one ascending pass.
+ */
+size_t rk_linear_logp_dw_workspace_size(int64_t n, int64_t H, int64_t V);
+rk_status rk_linear_logp_dw(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                            const int32_t *cu_seqlens, int32_t num_seqs,
+                            int64_t T, int64_t H, int64_t V,
+                            const float *lse, const float *grad_logp,
+                            const int64_t *row_order, int64_t n_order, float *dW,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * rk_linear_logp without a workspace argument, for callers that cannot
  * allocate device memory.  (No counterpart in the pages: this is an interface
  * convenience, not part of the method.)  Such callers include programs whose

@@ -28,7 +28,7 @@ __all__ = [
     "logp_from_logits",
     "linear_logp_bwd", "linear_logp_bwd_workspace_size", "linear_logp_bwd_min_workspace_size",
     "lm_head", "logp_from_logits_bwd", "grpo_token_loss", "linear_greedy",
-    "linear_greedy_workspace_size",
+    "linear_greedy_workspace_size", "linear_logp_dw", "linear_logp_dw_workspace_size",
     "get_device_error", "selftest_wait_timeout", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT",
 ]
 
@@ -91,6 +91,11 @@ def load_library() -> ctypes.CDLL:
     lib.rk_linear_greedy_workspace_size.restype = sz
     lib.rk_linear_greedy.argtypes = [vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, sz, vp]
     lib.rk_linear_greedy.restype = ctypes.c_int
+    lib.rk_linear_logp_dw_workspace_size.argtypes = [i64, i64, i64]
+    lib.rk_linear_logp_dw_workspace_size.restype = sz
+    lib.rk_linear_logp_dw.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, i64, vp, vp,
+                                      sz, vp]
+    lib.rk_linear_logp_dw.restype = ctypes.c_int
     lib.rk_selftest_wait_timeout.argtypes = [i64, vp]
     lib.rk_selftest_wait_timeout.restype = ctypes.c_int
     lib.rk_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
@@ -326,6 +331,43 @@ def linear_greedy(h: torch.Tensor, W: torch.Tensor, cu_seqlens: torch.Tensor | N
                               _stream_handle(stream, h.device))
     _check(st, "rk_linear_greedy")
     return token, logp, lse
+
+
+def linear_logp_dw_workspace_size(n: int, H: int, V: int) -> int:
+    return int(load_library().rk_linear_logp_dw_workspace_size(n, H, V))
+
+
+def linear_logp_dw(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
+                   grad_logp: torch.Tensor, cu_seqlens: torch.Tensor | None = None, *,
+                   row_order: torch.Tensor | None = None, dW: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None,
+                   stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """dW fp32 ``[V, H]`` summed over the active rows in canonical order
+    (``row_order``, int64 physical row indices; ascending rows by default)."""
+    lib = load_library()
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    T, H = h.shape
+    V = W.shape[0]
+    if W.shape[1] != H or W.device != h.device:
+        raise ValueError("W must be [V, H] on h's device")
+    cu, ns = _rows(targets, cu_seqlens, T, h.device)
+    _need(lse, "lse", torch.float32, 1)
+    _need(grad_logp, "grad_logp", torch.float32, 1)
+    n = T
+    if row_order is not None:
+        _need(row_order, "row_order", torch.int64, 1)
+        n = row_order.numel()
+    if dW is None:
+        dW = torch.empty((V, H), dtype=torch.float32, device=h.device)
+    if workspace is None:
+        need = int(lib.rk_linear_logp_dw_workspace_size(n, H, V))
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
+    st = lib.rk_linear_logp_dw(_ptr(h), _ptr(W), _ptr(targets), _ptr(cu), ns, T, H, V, _ptr(lse),
+                               _ptr(grad_logp), _ptr(row_order), n, _ptr(dW), _ptr(workspace),
+                               workspace.numel(), _stream_handle(stream, h.device))
+    _check(st, "rk_linear_logp_dw")
+    return dW
 
 
 def selftest_wait_timeout(limit_ns: int, stream: torch.cuda.Stream | None = None) -> None:

@@ -33,7 +33,9 @@
 //   kDz   dZ = g exp(z - lse) rounded to bf16 (0 on inactive rows);
 //   kDh   dh = g W[target] - acc in fp32 (0 on inactive rows);
 //   kLogits  z rounded to bf16 (the dense path's lm_head);
-//   kGreedy  kFwd plus the lowest column holding the tile maximum.
+//   kGreedy  kFwd plus the lowest column holding the tile maximum;
+//   kDw   dW[v, :] = sum over canonical tokens with target v (in canonical
+//         order, fp32) of g h  -  (dZ^T h)[v, :].
 // A second small kernel (linear_logp_merge) folds the forward partials of a
 // row in a fixed order into lse and logp.
 //
@@ -71,7 +73,9 @@ constexpr int kGroupNDh = 16;  // raster group (in H tiles) of the dh GEMM
 // kFwd: forward partials; kDz: backward GEMM 1; kDh: backward GEMM 2;
 // kLogits: the dense path's lm_head (z stored as bf16); kGreedy: kFwd plus
 // each tile's argmax column (greedy decoding).
-enum Mode { kFwd = 0, kDz = 1, kDh = 2, kLogits = 3, kGreedy = 4 };
+// kDw: the weight gradient, dW = S - dZ^T h over canonical tokens (A = dZ and
+// B = h both read MN-major), S the one-hot term added in the epilogue.
+enum Mode { kFwd = 0, kDz = 1, kDh = 2, kLogits = 3, kGreedy = 4, kDw = 5 };
 
 // full / tmem_empty / drain are used in the even CTA only; empty and
 // tmem_full in both (the MMA commits are multicast to the pair).
@@ -101,6 +105,12 @@ struct TileArgs {
     float2 *part;  // [rows][num_n]
     float *ztgt;   // [rows]
     int32_t *pidx; // kGreedy: [rows][num_n] column of each tile's maximum
+    // kDw (rows = vocabulary, columns = H, K = canonical tokens)
+    const uint16_t *hc;      // [n, H] canonical h
+    const float *gc;         // [n] canonical g
+    const int32_t *dw_val;   // sorted canonical token indices
+    const int32_t *dw_begin, *dw_end;  // [V] range of each target
+    float *dw;               // [V, H] output
     // kDz
     const float *lse;   // [T] (global)
     const float *grad;  // [T] (global)
@@ -122,7 +132,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 template <int MODE>
 __device__ __forceinline__ void tile_coords(int64_t tile, const TileArgs &a, int &mb, int &nb) {
-    if constexpr (MODE == kDh) {
+    if constexpr (MODE == kDh || MODE == kDw) {
         // groups of kGroupNDh H tiles; inside a group, row blocks outer: CTAs
         // running together share A (dZ rows) and walk W's K (vocabulary) rows
         // in step
@@ -150,8 +160,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       const TileArgs a) {
     // kDh: B is W read as [K = vocabulary rows, N = H columns] (N contiguous,
     // "MN-major"), staged as two 64-column boxes of BK rows per CTA.
-    constexpr bool kBmn = (MODE == kDh);
-    constexpr uint32_t kIdesc = idesc_bf16_f32(2 * BM, BN, false, kBmn);
+    constexpr bool kBmn = (MODE == kDh || MODE == kDw);
+    constexpr bool kAmn = (MODE == kDw);
+    constexpr uint32_t kIdesc = idesc_bf16_f32(2 * BM, BN, kAmn, kBmn);
     constexpr uint32_t kBBoxBytes = BK * 64 * 2;  // one 64-column MN-major box
     // Descriptor strides.  K-major, 128B swizzle: 8-row groups 1024 B apart;
     // the next 16-wide K slice starts 32 B further.  MN-major, 128B swizzle:
@@ -159,6 +170,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // apart (stride offset); the next 16-row K slice starts 16*128 B further.
     constexpr uint32_t kBLbo = kBmn ? kBBoxBytes : 16;
     constexpr uint32_t kBStepK = kBmn ? (UK * 128) : (UK * 2);
+    constexpr uint32_t kALbo = kAmn ? kBBoxBytes : 16;
+    constexpr uint32_t kAStepK = kAmn ? (UK * 128) : (UK * 2);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -216,10 +229,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tile_coords<MODE>(tile, a, mb, nb);
                 const int arow = mb * 2 * BM + (int)rank * BM;     // this CTA's A rows
                 const int bn0 = nb * BN + (int)rank * (BN / 2);    // this CTA's B rows / H columns
-                int nbox0 = 0, nbox1 = 0;
+                int nbox0 = 0, nbox1 = 0;    // B boxes of CTA 0 / 1 (MN-major)
+                int abox0 = 1, abox1 = 1;    // A boxes of CTA 0 / 1 (MN-major: up to 2)
                 if constexpr (kBmn) {
                     nbox0 = max(0, min(2, (a.H - nb * BN) / 64));
                     nbox1 = max(0, min(2, (a.H - nb * BN - BN / 2) / 64));
+                }
+                if constexpr (kAmn) {
+                    const int v0 = mb * 2 * BM;
+                    abox0 = max(0, min(2, (a.V - v0 + 63) / 64));
+                    abox1 = max(0, min(2, (a.V - v0 - BM + 63) / 64));
                 }
                 for (int kb = 0; kb < a.num_k; ++kb) {
                     if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort, a.err)) {
@@ -229,11 +248,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t fb = mapa_shared(smem_u32(&ctl->full[s]), 0);
                     const uint32_t sa = sbase + (uint32_t)(s * kStageBytes);
                     if (rank == 0) {
-                        const uint32_t bytes = kBmn ? (uint32_t)(2 * kABytes + (nbox0 + nbox1) * (int)kBBoxBytes)
-                                                    : (uint32_t)(2 * kStageBytes);
+                        uint32_t bytes = (uint32_t)(2 * kStageBytes);
+                        if constexpr (kAmn)
+                            bytes = (uint32_t)((abox0 + abox1 + nbox0 + nbox1) * (int)kBBoxBytes);
+                        else if constexpr (kBmn)
+                            bytes = (uint32_t)(2 * kABytes + (nbox0 + nbox1) * (int)kBBoxBytes);
                         mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), bytes);
                     }
-                    if constexpr (kBmn) {
+                    if constexpr (kAmn) {
+                        const int abox = rank == 0 ? abox0 : abox1;
+                        for (int j = 0; j < abox; ++j)
+                            tma_load_2d_pair(sa + j * kBBoxBytes, &tmA, fb, arow + j * 64, kb * BK);
+                        const int nbox = rank == 0 ? nbox0 : nbox1;
+                        for (int j = 0; j < nbox; ++j)
+                            tma_load_2d_pair(sa + kABytes + j * kBBoxBytes, &tmB, fb, bn0 + j * 64,
+                                             kb * BK);
+                    } else if constexpr (kBmn) {
                         tma_load_2d_pair(sa, &tmA, fb, kb * BK, arow);
                         const int nbox = rank == 0 ? nbox0 : nbox1;
                         for (int j = 0; j < nbox; ++j)
@@ -281,11 +311,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t sa = sbase + (uint32_t)(s * kStageBytes);
-                    const uint64_t ad = smem_desc_sw128(sa, 16, 1024);
+                    const uint64_t ad = smem_desc_sw128(sa, kALbo, 1024);
                     const uint64_t bd = smem_desc_sw128(sa + kABytes, kBLbo, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BK / UK; ++kk) {
-                        mma_bf16_ss_pair(d, ad + (uint64_t)((kk * UK * 2) >> 4),
+                        mma_bf16_ss_pair(d, ad + (uint64_t)((kk * kAStepK) >> 4),
                                          bd + (uint64_t)((kk * kBStepK) >> 4), kIdesc,
                                          (kb | kk) != 0 ? 1u : 0u);
                     }
@@ -443,6 +473,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 if (c0 + j < valid)
                                     drow[c0 + j] = (uint16_t)((j & 1) ? (pk[j >> 1] >> 16) : (pk[j >> 1] & 0xFFFFu));
                         }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(empty_bar);
+            } else if constexpr (MODE == kDw) {
+                // lrow is a vocabulary row; its one-hot term runs over the
+                // canonical tokens whose target it is, in canonical order
+                const bool vrow = lrow < a.V;
+                const int32_t b0 = vrow ? a.dw_begin[lrow] : 0;
+                const int32_t b1 = vrow ? a.dw_end[lrow] : 0;
+                const int hvalid = min(BN, a.H - n0);
+                if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
+                tc_fence_after();
+                const uint32_t taddr = tmem + lane_off + (uint32_t)(b * BN);
+                float *orow = a.dw + lrow * (int64_t)a.H + n0;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
+                    tmem_ld_wait();
+                    if (vrow && c * 32 < hvalid) {
+                        float sacc[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) sacc[j] = 0.f;
+                        for (int32_t i = b0; i < b1; ++i) {
+                            const int32_t tok = a.dw_val[i];
+                            const float w = a.gc[tok];
+                            const uint4 *src =
+                                reinterpret_cast<const uint4 *>(a.hc + (int64_t)tok * a.H + n0 + c * 32);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const uint4 v4 = __ldg(src + q);
+                                const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const int j = q * 8 + u * 2;
+                                    sacc[j] = __fmaf_rn(w, bf16_lo(w4[u]), sacc[j]);
+                                    sacc[j + 1] = __fmaf_rn(w, bf16_hi(w4[u]), sacc[j + 1]);
+                                }
+                            }
+                        }
+                        float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(__fsub_rn(sacc[4 * q], __uint_as_float(r[4 * q])),
+                                                 __fsub_rn(sacc[4 * q + 1], __uint_as_float(r[4 * q + 1])),
+                                                 __fsub_rn(sacc[4 * q + 2], __uint_as_float(r[4 * q + 2])),
+                                                 __fsub_rn(sacc[4 * q + 3], __uint_as_float(r[4 * q + 3])));
                     }
                 }
                 tc_fence_before();
@@ -780,6 +859,103 @@ cudaError_t launch_lm_head(const uint16_t *h, const uint16_t *W, int64_t T, int6
     a.dz = logits;
     a.ldz = ld;
     return run_tiles<kLogits>(tmA, tmB, a, di, st);
+}
+
+size_t linear_dw_workspace_bytes(int64_t n, int64_t H, int64_t V) {
+    if (n <= 0) return 0;
+    const size_t ln = (size_t)n;
+    size_t b = 0;
+    b += round256(ln * 8) + round256(8);                    // crow, n_active
+    b += round256(ln * (size_t)H * 2);                      // hc
+    b += 2 * round256(ln * 4) + round256(ln * 8);           // gc, lsec, tgtc
+    b += 4 * round256(ln * 4);                              // sort buffers
+    b += 2 * round256((size_t)V * 4);                       // begin, end
+    b += round256(ln * (size_t)ld_dz(V) * 2);               // dZ
+    return b;
+}
+
+cudaError_t launch_linear_dw(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                             const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
+                             const float *lse, const float *grad, const int64_t *order, int64_t n,
+                             float *dW, void *workspace, const DeviceInfo &di, cudaStream_t st) {
+    if (n == 0) return cudaMemsetAsync(dW, 0, (size_t)V * (size_t)H * sizeof(float), st);
+    uint8_t *w = reinterpret_cast<uint8_t *>(workspace);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t *p = w + off;
+        off += round256(bytes);
+        return p;
+    };
+    const size_t ln = (size_t)n;
+    DwBuffers bf;
+    bf.crow = reinterpret_cast<int64_t *>(take(ln * 8));
+    bf.n_active = reinterpret_cast<int64_t *>(take(8));
+    bf.hc = reinterpret_cast<uint16_t *>(take(ln * (size_t)H * 2));
+    bf.gc = reinterpret_cast<float *>(take(ln * 4));
+    bf.lsec = reinterpret_cast<float *>(take(ln * 4));
+    bf.tgtc = reinterpret_cast<int64_t *>(take(ln * 8));
+    bf.key0 = reinterpret_cast<int32_t *>(take(ln * 4));
+    bf.val0 = reinterpret_cast<int32_t *>(take(ln * 4));
+    bf.key1 = reinterpret_cast<int32_t *>(take(ln * 4));
+    bf.val1 = reinterpret_cast<int32_t *>(take(ln * 4));
+    bf.begin = reinterpret_cast<int32_t *>(take((size_t)V * 4));
+    bf.end = reinterpret_cast<int32_t *>(take((size_t)V * 4));
+    bf.ldz = ld_dz(V);
+    bf.dz = reinterpret_cast<uint16_t *>(take(ln * (size_t)bf.ldz * 2));
+
+    cudaError_t e = launch_dw_prep(h, targets, cu, num_seqs, T, H, V, lse, grad, order, n, bf, di, st);
+    if (e != cudaSuccess) return e;
+
+    // dZ over the canonical tokens (every position past the active count has
+    // target -1 and so gives a zero row)
+    CUtensorMap tmHc, tmW, tmDzT, tmHcT;
+    if (!encode_tmap_bf16_2d(&tmHc, bf.hc, (uint64_t)H, (uint64_t)n, (uint64_t)H * 2, BK, BM, true))
+        return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16_2d(&tmW, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2, true))
+        return cudaErrorInvalidValue;
+    TileArgs a{};
+    a.targets = bf.tgtc;
+    a.cu = nullptr;
+    a.num_seqs = 0;
+    a.row0 = 0;
+    a.rows = n;
+    a.V = (int32_t)V;
+    a.H = (int32_t)H;
+    a.err = di.err;
+    a.lse = bf.lsec;
+    a.grad = bf.gc;
+    a.dz = bf.dz;
+    a.ldz = bf.ldz;
+    a.num_m = (int32_t)((n + 2 * BM - 1) / (2 * BM));
+    a.num_n = (int32_t)((V + BN - 1) / BN);
+    a.num_k = (int32_t)(H / BK);
+    e = run_tiles<kDz>(tmHc, tmW, a, di, st);
+    if (e != cudaSuccess) return e;
+
+    // dW = S - dZ^T h: rows = vocabulary, columns = H, K = canonical tokens;
+    // A = dZ read as [K][M], B = h read as [K][N], both in 64x64 boxes
+    if (!encode_tmap_bf16_2d(&tmDzT, bf.dz, (uint64_t)V, (uint64_t)n, (uint64_t)bf.ldz * 2, 64, BK,
+                             true))
+        return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16_2d(&tmHcT, bf.hc, (uint64_t)H, (uint64_t)n, (uint64_t)H * 2, 64, BK, true))
+        return cudaErrorInvalidValue;
+    TileArgs d{};
+    d.targets = nullptr;
+    d.rows = V;
+    d.V = (int32_t)V;
+    d.H = (int32_t)H;
+    d.err = di.err;
+    d.hc = bf.hc;
+    d.gc = bf.gc;
+    const int bits = [&] { int b = 1; while ((int64_t(1) << b) < V) ++b; return b; }();
+    d.dw_val = (bits % 2 == 0) ? bf.val0 : bf.val1;
+    d.dw_begin = bf.begin;
+    d.dw_end = bf.end;
+    d.dw = dW;
+    d.num_m = (int32_t)((V + 2 * BM - 1) / (2 * BM));
+    d.num_n = (int32_t)((H + BN - 1) / BN);
+    d.num_k = (int32_t)((n + BK - 1) / BK);
+    return run_tiles<kDw>(tmDzT, tmHcT, d, di, st);
 }
 
 int64_t linear_bwd_chunk_quantum() { return BM; }

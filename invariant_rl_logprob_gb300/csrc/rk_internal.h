@@ -66,6 +66,29 @@ cudaError_t launch_grpo_token(const float *logp, const float *logp_old, const fl
                               float scale, float *loss, float *grad, float *ratio, float *kl,
                               const DeviceInfo &di, cudaStream_t st);
 
+// ---- linear_logp weight gradient (dw_prep.cu, linear_logp_tc.cu) ----
+struct DwBuffers {
+    int64_t *crow;      // [n] physical row of each canonical token
+    int64_t *n_active;  // [1] number of canonical tokens
+    uint16_t *hc;       // [n, H] bf16 canonical h (zeros past n_active)
+    float *gc;          // [n] canonical upstream gradient (0 past n_active)
+    float *lsec;        // [n] canonical lse
+    int64_t *tgtc;      // [n] canonical targets (-1 past n_active)
+    int32_t *key0, *val0, *key1, *val1;  // [n] sort buffers
+    int32_t *begin, *end;                // [V] each target's range in the sorted list
+    uint16_t *dz;       // [n, ldz] bf16 canonical g * softmax
+    int64_t ldz;
+};
+size_t linear_dw_workspace_bytes(int64_t n, int64_t H, int64_t V);
+cudaError_t launch_dw_prep(const uint16_t *h, const int64_t *targets, const int32_t *cu,
+                           int num_seqs, int64_t T, int64_t H, int64_t V, const float *lse,
+                           const float *grad, const int64_t *order, int64_t n, const DwBuffers &b,
+                           const DeviceInfo &di, cudaStream_t st);
+cudaError_t launch_linear_dw(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                             const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
+                             const float *lse, const float *grad, const int64_t *order, int64_t n,
+                             float *dW, void *workspace, const DeviceInfo &di, cudaStream_t st);
+
 // ---- linear_logp backward (linear_logp_tc.cu) ----
 size_t linear_bwd_chunk_bytes(int64_t rows, int64_t V);
 int64_t linear_bwd_chunk_quantum();

@@ -1,0 +1,92 @@
+"""dW of linear_logp on the GPU: parity with the fp64 oracle, the one-hot
+term's edge cases, and bitwise invariance over the same complete sample set
+in canonical order (issue #244 "[WS1 Test] ...", Workstream 3)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_rl_logprob_gb300 import contract, synth
+from tests.helpers import DEV, bits_np, cuda, same_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rk():
+    from invariant_rl_logprob_gb300 import build
+    build.build()
+    import invariant_rl_logprob_gb300 as m
+    m.load_library()
+    m.get_device_error()
+    return m
+
+
+def _case(T, H, V, seed, w_std=0.05):
+    gen = synth.generator(seed)
+    W = synth.normal_bf16(gen, (V, H), w_std)
+    h = synth.normal_bf16(gen, (T, H), 1.0)
+    tg = synth.uniform_targets(gen, T, V)
+    g = torch.randn(T, generator=gen, dtype=torch.float32)
+    return h, W, tg, g
+
+
+def _gpu_dw(rk, h, W, tg, g, cu=None, order=None):
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    _, lse = rk.linear_logp(hd, Wd, tgd, cuda(cu))
+    return rk.linear_logp_dw(hd, Wd, tgd, lse, gd, cuda(cu), row_order=cuda(order))
+
+
+@pytest.mark.parametrize("T,H,V", [(64, 256, 4096), (300, 128, 1001), (129, 192, 700), (7, 64, 5)])
+def test_dw_vs_oracle(rk, T, H, V):
+    h, W, tg, g = _case(T, H, V, 5000 + T + V)
+    tg[::11] = -100
+    dW = _gpu_dw(rk, h, W, tg, g).cpu().numpy()
+    ref = oracle.linear_logp_dw(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy())
+    chk = contract.check_gradient_accuracy(dW, ref)
+    assert chk.passed, chk
+    assert rk.get_device_error() == 0
+
+
+def test_dw_all_tokens_one_target_and_empty(rk):
+    h, W, tg, g = _case(200, 128, 1000, 77)
+    tg[:] = 513                                            # one bucket of 200 tokens
+    dW = _gpu_dw(rk, h, W, tg, g).cpu().numpy()
+    ref = oracle.linear_logp_dw(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy())
+    assert contract.check_gradient_accuracy(dW, ref).passed
+    tg[:] = -100                                           # no active token
+    dW0 = _gpu_dw(rk, h, W, tg, g).cpu()
+    assert torch.all(dW0 == 0)
+
+
+def test_dw_canonical_order_invariance(rk):
+    # the same sample set, physical layouts: packed, padded (left/right), with
+    # neighbours outside the set redrawn, sequences reversed -- each given the
+    # canonical order (sequence id, position) of its active tokens
+    pool = synth.make_pool(128, 3000, [40, 70, 25, 33], seed=90, with_grad=True)
+    W = cuda(pool.W)
+
+    def dw_of(lay, seqs):
+        order = torch.tensor([r for i in seqs for r in lay.rows_of[i]], dtype=torch.int64)
+        h, tg, g = cuda(lay.h), cuda(lay.targets), cuda(lay.g)
+        _, lse = rk.linear_logp(h, W, tg)
+        return rk.linear_logp_dw(h, W, tg, lse, g, row_order=cuda(order)).cpu()
+
+    seqs = [0, 1, 2, 3]
+    base = dw_of(synth.packed(pool, seqs), seqs)
+    variants = [synth.padded(pool, seqs, 80, side="right"), synth.padded(pool, seqs, 80, side="left"),
+                synth.packed(pool, [3, 2, 1, 0], lead_pad=37), synth.packed(pool, [2, 0, 3, 1])]
+    for lay in variants:
+        assert same_bits(dw_of(lay, seqs), base), lay.description
+    # and against the oracle in the same canonical order
+    lay = synth.packed(pool, seqs)
+    ref = oracle.linear_logp_dw(bits_np(lay.h), bits_np(pool.W), lay.targets.numpy(),
+                                np.nan_to_num(lay.g.double().numpy()))
+    assert contract.check_gradient_accuracy(base.numpy(), ref).passed
+
+
+def test_dw_run_to_run(rk):
+    h, W, tg, g = _case(500, 256, 4096, 31)
+    a = _gpu_dw(rk, h, W, tg, g)
+    b = _gpu_dw(rk, h, W, tg, g)
+    assert same_bits(a, b)
