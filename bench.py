@@ -11,7 +11,7 @@ device time, inputs resident in HBM.  h (512 MB) and W (1.05 GB) exceed the
 126 MB L2, so nothing carries over between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-    python bench.py --case {fwd,bwd,logits} [--shape T,H,V] [--reps R]
+    python bench.py --case {fwd,bwd,logits,dw} [--shape T,H,V] [--reps R]
 
 `--case` runs one operator a few times on a small workload (for profiler
 captures; default T=2048, H=4096, V=32000: W and the logits exceed L2) and
@@ -631,6 +631,12 @@ def run_case(args) -> None:
         if args.case == "fwd":
             fn = lambda: rk.linear_logp(h, W, tg)
             flops = 2.0 * T * H * V
+        elif args.case == "dw":
+            ws = torch.empty(rk.linear_logp_dw_workspace_size(T, H, V), dtype=torch.uint8,
+                             device=dev)
+            dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+            fn = lambda: rk.linear_logp_dw(h, W, tg, lse, g, dW=dW, workspace=ws)
+            flops = 4.0 * T * H * V
         else:
             ws = torch.empty(rk.linear_logp_bwd_workspace_size(T, H, V), dtype=torch.uint8,
                              device=dev)
@@ -663,7 +669,7 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the separate timing of the widened rows")
-    ap.add_argument("--case", choices=["fwd", "bwd", "logits"], default=None)
+    ap.add_argument("--case", choices=["fwd", "bwd", "logits", "dw"], default=None)
     ap.add_argument("--shape", default="2048,4096,32000")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()

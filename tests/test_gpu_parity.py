@@ -269,3 +269,20 @@ def test_grpo_shape_sampled_rows(rk):
     ref_dh = oracle_bwd(hb, Wb, lay.targets.numpy(), lay.g.double().numpy(), rows=rows)
     _check_bwd(dh.cpu()[rows], ref_dh, "grpo bwd sampled")
     assert rk.get_device_error() == 0
+
+
+@pytest.mark.slow
+def test_qwen_shape_padded_sampled_rows(rk):
+    # [8, 2048] right-padded batch of the Qwen-shaped pool (pads NaN, target
+    # -100): sampled active rows against the oracle, inactive rows exactly 0
+    pool = synth.qwen_pool()
+    lay = synth.padded(pool, list(range(8)), 2048)
+    logp, lse = rk.linear_logp(cuda(lay.h), cuda(pool.W), cuda(lay.targets))
+    act = oracle.active_rows(lay.targets.numpy())
+    rows = [r for r in synth.sample_rows(lay.T, 96, seed=3) if act[r]][:48]
+    ref_logp, ref_lse = oracle_linear(bits_np(lay.h), bits_np(pool.W), lay.targets.numpy(),
+                                      rows=rows)
+    _check_fwd(logp.cpu()[rows], lse.cpu()[rows], ref_logp, ref_lse, "qwen padded sampled")
+    lp = logp.cpu()
+    assert torch.all(lp[~torch.from_numpy(act)] == 0)
+    assert torch.all(torch.isfinite(lp))
