@@ -67,13 +67,6 @@ bool encode_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uin
                      row_stride_bytes, box_inner, box_outer, sw128);
 }
 
-bool encode_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
-                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
-                        bool sw128) {
-    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, inner, outer,
-                     row_stride_bytes, box_inner, box_outer, sw128);
-}
-
 void record_cuda_error(int e) { g_last_cuda_error = e; }
 
 cudaError_t current_device_info(DeviceInfo *di) {

@@ -73,3 +73,38 @@ def test_argument_errors_return_before_any_launch(lib):
     g.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int32] + [ctypes.c_int64] * 2 + \
         [ctypes.c_void_p] * 3
     assert g(None, None, None, 0, 5, 0, None, None, None) == 1                         # V = 0
+
+
+def test_argument_errors_of_the_widened_rows(lib):
+    vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    lh = lib.rk_lm_head
+    lh.restype = ctypes.c_int
+    lh.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp]
+    assert lh(None, None, -1, 64, 10, None, 16, None) == 1          # T < 0
+    assert lh(None, None, 0, 64, 10, None, 16, None) == 0           # T = 0: nothing to do
+    fake = ctypes.c_void_p(4096)                                     # never dereferenced
+    assert lh(fake, fake, 4, 64, 10, fake, 8, None) == 1            # ld < V
+    assert lh(fake, fake, 4, 96, 10, fake, 16, None) == 2           # H % 64 != 0
+    gl = lib.rk_grpo_token_loss
+    gl.restype = ctypes.c_int
+    gl.argtypes = [vp] * 6 + [i32, i64, f32, f32, f32, f32] + [vp] * 5
+    assert gl(fake, fake, None, fake, fake, None, 0, 8, 1.5, 0.2, 0.0, 1.0, fake, fake, None, None, None) == 1
+    assert gl(fake, fake, None, fake, fake, None, 0, 8, 0.2, 0.2, -1.0, 1.0, fake, fake, None, None, None) == 1
+    assert gl(fake, None, None, fake, fake, None, 0, 8, 0.2, 0.2, 0.0, 1.0, fake, fake, None, None, None) == 1
+    dw = lib.rk_linear_logp_dw
+    dw.restype = ctypes.c_int
+    dw.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, i64, vp, vp, sz, vp]
+    assert dw(fake, fake, fake, None, 0, 8, 64, 100, fake, fake, fake, -1, fake, fake, 1 << 30, None) == 1
+    assert dw(fake, fake, fake, None, 0, 8, 64, 100, fake, fake, None, 0, fake, None, 0, None) == 3
+    q = lib.rk_linear_logp_dw_workspace_size
+    q.restype = sz
+    q.argtypes = [i64, i64, i64]
+    assert q(0, 64, 100) == 0 and q(100, 64, 1000) > 100 * 1008 * 2
+    gr = lib.rk_linear_greedy
+    gr.restype = ctypes.c_int
+    gr.argtypes = [vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, sz, vp]
+    assert gr(fake, fake, None, 0, 8, 64, 100, fake, fake, None, None, 0, None) == 3
+    st = lib.rk_selftest_wait_timeout
+    st.restype = ctypes.c_int
+    st.argtypes = [i64, vp]
+    assert st(0, None) == 1 and st(20_000_000_000, None) == 1

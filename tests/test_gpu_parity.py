@@ -286,3 +286,18 @@ def test_qwen_shape_padded_sampled_rows(rk):
     lp = logp.cpu()
     assert torch.all(lp[~torch.from_numpy(act)] == 0)
     assert torch.all(torch.isfinite(lp))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T,V", [(1024, 152064), (65536, 32000)])
+def test_logits_path_large_sampled(rk, T, V):
+    # the Qwen vocabulary (not a multiple of 256) and a 4.2 GB batch: sampled
+    # rows against the oracle, properties on every row
+    z, tg, _ = synth.logits_batch(T=T, V=V, seed=T + V)
+    logp, lse = rk.logp_from_logits(cuda(z), cuda(tg))
+    rows = synth.sample_rows(T, 64, seed=V)
+    ref_logp, ref_lse = oracle_logits(bits_np(z), tg.numpy(), rows=rows)
+    _check_fwd(logp.cpu()[rows], lse.cpu()[rows], ref_logp, ref_lse, f"logits T={T} V={V}")
+    lp = logp.cpu()
+    assert torch.all(torch.isfinite(lp)) and torch.all(lp <= 0)
+    assert rk.get_device_error() == 0
