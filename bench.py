@@ -52,9 +52,9 @@ WORKLOAD = ("grpo_fwd_bwd: linear_logp fwd+bwd T=65536 (64x1024) H=4096 V=128256
 #  --warmup 3 --no-cpu-baseline --no-rows`, one pass per launch), recorded with
 # the SHA-1 of the kernel source; reported only while the source still matches.
 TRAFFIC_RECORD = {
-    "source_sha1": "3bf799eabbf16c340be346d2d94f5973e9857dcb",
-    "bytes_per_step": 465151402496,
-    "per_launch_gb": {"fwd": 153.75, "dZ": 90.30, "dh": 221.10},
+    "source_sha1": "d7d43f3e9cf3af13db7a46f992c8ff47d273003d",
+    "bytes_per_step": 547005491968,
+    "per_launch_gb": {"fwd": 176.48, "dZ": 136.22, "dh": 234.31},
 }
 # Unique bytes a step has to move: forward h + W + partials; dZ GEMM h + W +
 # dZ written; dh GEMM dZ + W read, dh written.
