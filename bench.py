@@ -339,7 +339,17 @@ def measure_rows(rk, pool, zs, peaks, dev, stream) -> dict:
                              "peak": peaks["bf16_tflops_sustained"],
                              "frac": tf / peaks["bf16_tflops_sustained"],
                              "algorithmic": "4*T*H*V flop (dZ recompute + dZ^T h)"}
-    del wsd, dW
+    # the whole backward (dh + dW) from one shared softmax pass, 6*T*H*V flop
+    dh = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ms = time_loop(lambda i: rk.linear_logp_bwd_full(h, W, tg, lse, g, dh=dh, dW=dW, workspace=wsd,
+                                                     stream=stream), 3, stream)
+    tf = 6.0 * T * H * V / (ms / 1e3) / 1e12
+    out["linear_logp_bwd_full"] = {"shape": [T, H, V], "ms_per_call": ms, "bound": "tensor",
+                                   "achieved": tf, "unit": "TFLOP/s",
+                                   "peak": peaks["bf16_tflops_sustained"],
+                                   "frac": tf / peaks["bf16_tflops_sustained"],
+                                   "algorithmic": "6*T*H*V flop (dZ + dh + dW GEMMs)"}
+    del wsd, dW, dh
     return out
 
 

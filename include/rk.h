@@ -238,6 +238,26 @@ rk_status rk_linear_logp_dw(const uint16_t *h, const uint16_t *W, const int64_t 
                             void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The whole backward of linear_logp in one call: dh (as rk_linear_logp_bwd)
+ * and dW (as rk_linear_logp_dw) from one shared g * softmax over the
+ * canonical tokens, so z is recomputed once instead of twice (8*T*H*V flop
+ * for forward + this call instead of 10*T*H*V).  dh is bitwise identical to
+ * rk_linear_logp_bwd's and dW to rk_linear_logp_dw's for the same inputs:
+ * each dh row is computed over the canonical rows and stored at its physical
+ * row; rows outside the canonical set get 0, active rows with targets >= V
+ * get NaN and RK_DEVERR_TARGET_RANGE.
+ *   arguments: as rk_linear_logp_dw, plus dh fp32 [T, H] (16-byte aligned);
+ *   workspace >= rk_linear_logp_dw_workspace_size(n, H, V) bytes.
+ */
+rk_status rk_linear_logp_bwd_full(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                                  const int32_t *cu_seqlens, int32_t num_seqs,
+                                  int64_t T, int64_t H, int64_t V,
+                                  const float *lse, const float *grad_logp,
+                                  const int64_t *row_order, int64_t n_order,
+                                  float *dh, float *dW,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * rk_linear_logp without a workspace argument, for callers that cannot
  * allocate device memory.  (No counterpart in the pages: this is an interface
  * convenience, not part of the method.)  Such callers include programs whose

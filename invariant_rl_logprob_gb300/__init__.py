@@ -29,6 +29,7 @@ __all__ = [
     "linear_logp_bwd", "linear_logp_bwd_workspace_size", "linear_logp_bwd_min_workspace_size",
     "lm_head", "logp_from_logits_bwd", "grpo_token_loss", "linear_greedy",
     "linear_greedy_workspace_size", "linear_logp_dw", "linear_logp_dw_workspace_size",
+    "linear_logp_bwd_full",
     "get_device_error", "selftest_wait_timeout", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT",
 ]
 
@@ -96,6 +97,9 @@ def load_library() -> ctypes.CDLL:
     lib.rk_linear_logp_dw.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, i64, vp, vp,
                                       sz, vp]
     lib.rk_linear_logp_dw.restype = ctypes.c_int
+    lib.rk_linear_logp_bwd_full.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, i64,
+                                            vp, vp, vp, sz, vp]
+    lib.rk_linear_logp_bwd_full.restype = ctypes.c_int
     lib.rk_selftest_wait_timeout.argtypes = [i64, vp]
     lib.rk_selftest_wait_timeout.restype = ctypes.c_int
     lib.rk_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
@@ -368,6 +372,42 @@ def linear_logp_dw(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, lse:
                                workspace.numel(), _stream_handle(stream, h.device))
     _check(st, "rk_linear_logp_dw")
     return dW
+
+
+def linear_logp_bwd_full(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor,
+                         lse: torch.Tensor, grad_logp: torch.Tensor,
+                         cu_seqlens: torch.Tensor | None = None, *,
+                         row_order: torch.Tensor | None = None, dh: torch.Tensor | None = None,
+                         dW: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                         stream: torch.cuda.Stream | None = None):
+    """(dh fp32 [T, H], dW fp32 [V, H]) from one shared softmax pass."""
+    lib = load_library()
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    T, H = h.shape
+    V = W.shape[0]
+    if W.shape[1] != H or W.device != h.device:
+        raise ValueError("W must be [V, H] on h's device")
+    cu, ns = _rows(targets, cu_seqlens, T, h.device)
+    _need(lse, "lse", torch.float32, 1)
+    _need(grad_logp, "grad_logp", torch.float32, 1)
+    n = T
+    if row_order is not None:
+        _need(row_order, "row_order", torch.int64, 1)
+        n = row_order.numel()
+    if dh is None:
+        dh = torch.empty((T, H), dtype=torch.float32, device=h.device)
+    if dW is None:
+        dW = torch.empty((V, H), dtype=torch.float32, device=h.device)
+    if workspace is None:
+        need = int(lib.rk_linear_logp_dw_workspace_size(n, H, V))
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
+    st = lib.rk_linear_logp_bwd_full(_ptr(h), _ptr(W), _ptr(targets), _ptr(cu), ns, T, H, V,
+                                     _ptr(lse), _ptr(grad_logp), _ptr(row_order), n, _ptr(dh),
+                                     _ptr(dW), _ptr(workspace), workspace.numel(),
+                                     _stream_handle(stream, h.device))
+    _check(st, "rk_linear_logp_bwd_full")
+    return dh, dW
 
 
 def selftest_wait_timeout(limit_ns: int, stream: torch.cuda.Stream | None = None) -> None:

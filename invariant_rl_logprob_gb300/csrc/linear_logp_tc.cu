@@ -119,6 +119,7 @@ struct TileArgs {
     // kDh
     const uint16_t *W;  // [V][H]
     float *dh;          // [T][H] (global)
+    const int64_t *out_rows;  // kDh over canonical rows: physical row of each (or null)
     int32_t H;
 };
 
@@ -532,16 +533,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const float g = active ? a.grad[grow] : 0.f;
                 const uint16_t *wrow = a.W + (active ? tgt : 0) * (int64_t)a.H + n0;
                 const int hvalid = min(BN, a.H - n0);  // a multiple of 64
+                // canonical rows scatter to their physical rows; padding
+                // positions (inactive) are not stored
+                const bool store = in_range && (a.out_rows == nullptr || active);
+                const int64_t orow_i = (a.out_rows == nullptr) ? grow : (active ? a.out_rows[grow] : 0);
                 if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
                 tc_fence_after();
                 const uint32_t taddr = tmem + lane_off + (uint32_t)(b * BN);
-                float *orow = a.dh + grow * (int64_t)a.H + n0;
+                float *orow = a.dh + orow_i * (int64_t)a.H + n0;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
                     tmem_ld_wait();
-                    if (in_range && c * 32 < hvalid) {
+                    if (store && c * 32 < hvalid) {
                         float o[32];
                         if (active) {
                             uint4 wv[4];
@@ -874,11 +879,48 @@ size_t linear_dw_workspace_bytes(int64_t n, int64_t H, int64_t V) {
     return b;
 }
 
+// Canonical backward: prep + dZ over the canonical tokens, then (if dh) the
+// dh GEMM scattered back to physical rows, then (if dW) the dW GEMM.
+static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                                      const int32_t *cu, int num_seqs, int64_t T, int64_t H,
+                                      int64_t V, const float *lse, const float *grad,
+                                      const int64_t *order, int64_t n, float *dh, float *dW,
+                                      void *workspace, const DeviceInfo &di, cudaStream_t st);
+
 cudaError_t launch_linear_dw(const uint16_t *h, const uint16_t *W, const int64_t *targets,
                              const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
                              const float *lse, const float *grad, const int64_t *order, int64_t n,
                              float *dW, void *workspace, const DeviceInfo &di, cudaStream_t st) {
-    if (n == 0) return cudaMemsetAsync(dW, 0, (size_t)V * (size_t)H * sizeof(float), st);
+    return canonical_backward(h, W, targets, cu, num_seqs, T, H, V, lse, grad, order, n, nullptr,
+                              dW, workspace, di, st);
+}
+
+cudaError_t launch_linear_bwd_full(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                                   const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
+                                   const float *lse, const float *grad, const int64_t *order,
+                                   int64_t n, float *dh, float *dW, void *workspace,
+                                   const DeviceInfo &di, cudaStream_t st) {
+    // rows outside the canonical set keep dh = 0; out-of-range targets get NaN
+    cudaError_t e = cudaMemsetAsync(dh, 0, (size_t)T * (size_t)H * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+    e = canonical_backward(h, W, targets, cu, num_seqs, T, H, V, lse, grad, order, n, dh, dW,
+                           workspace, di, st);
+    if (e != cudaSuccess) return e;
+    if (T > 0) {
+        linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(targets, cu, num_seqs, T,
+                                                              (int32_t)V, (int32_t)H, dh, di.err);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                                      const int32_t *cu, int num_seqs, int64_t T, int64_t H,
+                                      int64_t V, const float *lse, const float *grad,
+                                      const int64_t *order, int64_t n, float *dh, float *dW,
+                                      void *workspace, const DeviceInfo &di, cudaStream_t st) {
+    if (n == 0)
+        return dW ? cudaMemsetAsync(dW, 0, (size_t)V * (size_t)H * sizeof(float), st) : cudaSuccess;
     uint8_t *w = reinterpret_cast<uint8_t *>(workspace);
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -931,6 +973,26 @@ cudaError_t launch_linear_dw(const uint16_t *h, const uint16_t *W, const int64_t
     a.num_k = (int32_t)(H / BK);
     e = run_tiles<kDz>(tmHc, tmW, a, di, st);
     if (e != cudaSuccess) return e;
+
+    if (dh) {
+        // dh over the canonical rows, K = V ascending, each row stored at its
+        // physical position (the same arithmetic per row as rk_linear_logp_bwd)
+        CUtensorMap tmDz, tmWmn;
+        if (!encode_tmap_bf16_2d(&tmDz, bf.dz, (uint64_t)V, (uint64_t)n, (uint64_t)bf.ldz * 2, BK,
+                                 BM, true))
+            return cudaErrorInvalidValue;
+        if (!encode_tmap_bf16_2d(&tmWmn, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, 64, BK, true))
+            return cudaErrorInvalidValue;
+        TileArgs q = a;
+        q.W = W;
+        q.dh = dh;
+        q.out_rows = bf.crow;
+        q.num_n = (int32_t)((H + BN - 1) / BN);
+        q.num_k = (int32_t)((V + BK - 1) / BK);
+        e = run_tiles<kDh>(tmDz, tmWmn, q, di, st);
+        if (e != cudaSuccess) return e;
+    }
+    if (!dW) return cudaSuccess;
 
     // dW = S - dZ^T h: rows = vocabulary, columns = H, K = canonical tokens;
     // A = dZ read as [K][M], B = h read as [K][N], both in 64x64 boxes

@@ -84,6 +84,11 @@ cudaError_t launch_linear_dw(const uint16_t *h, const uint16_t *W, const int64_t
                              const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
                              const float *lse, const float *grad, const int64_t *order, int64_t n,
                              float *dW, void *workspace, const DeviceInfo &di, cudaStream_t st);
+cudaError_t launch_linear_bwd_full(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                                   const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
+                                   const float *lse, const float *grad, const int64_t *order,
+                                   int64_t n, float *dh, float *dW, void *workspace,
+                                   const DeviceInfo &di, cudaStream_t st);
 
 // ---- linear_logp backward (linear_logp_tc.cu) ----
 size_t linear_bwd_chunk_bytes(int64_t rows, int64_t V);

@@ -90,3 +90,27 @@ def test_dw_run_to_run(rk):
     a = _gpu_dw(rk, h, W, tg, g)
     b = _gpu_dw(rk, h, W, tg, g)
     assert same_bits(a, b)
+
+
+def test_full_backward_matches_separate_calls(rk):
+    # one shared softmax pass gives the same dh as rk_linear_logp_bwd and the
+    # same dW as rk_linear_logp_dw, bit for bit; masked rows 0, bad targets NaN
+    pool = synth.make_pool(192, 2500, [50, 90, 41], seed=93, with_grad=True)
+    lay = synth.packed(pool, [0, 1, 2], lead_pad=9)
+    tg = lay.targets.clone()
+    tg[30] = 2500                                          # out of range: NaN row + error bit
+    h, W, tgd, cu, g = cuda(lay.h), cuda(pool.W), cuda(tg), cuda(lay.cu_seqlens), cuda(lay.g)
+    _, lse = rk.linear_logp(h, W, tgd, cu)
+    rk.get_device_error()
+    dh_sep = rk.linear_logp_bwd(h, W, tgd, lse, g, cu)
+    dw_sep = rk.linear_logp_dw(h, W, tgd, lse, g, cu)
+    assert rk.get_device_error() & rk.DEVERR_TARGET_RANGE
+    dh_full, dw_full = rk.linear_logp_bwd_full(h, W, tgd, lse, g, cu)
+    assert rk.get_device_error() & rk.DEVERR_TARGET_RANGE
+    assert same_bits(dh_full, dh_sep) and same_bits(dw_full, dw_sep)
+    d = dh_full.cpu()
+    assert torch.all(d[:9] == 0) and torch.all(torch.isnan(d[30]))
+    act = oracle.active_rows(tg.numpy(), lay.cu_seqlens.numpy()) & (tg.numpy() < 2500)
+    ref = oracle.linear_logp_dw(bits_np(lay.h), bits_np(pool.W), np.where(act, tg.numpy(), -100),
+                                np.nan_to_num(lay.g.double().numpy()), lay.cu_seqlens.numpy())
+    assert contract.check_gradient_accuracy(dw_full.cpu().numpy(), ref).passed
