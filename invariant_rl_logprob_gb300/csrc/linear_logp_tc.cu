@@ -75,7 +75,10 @@ constexpr int kGroupNDh = 16;  // raster group (in H tiles) of the dh GEMM
 // each tile's argmax column (greedy decoding).
 // kDw: the weight gradient, dW = S - dZ^T h over canonical tokens (A = dZ and
 // B = h both read MN-major), S the one-hot term added in the epilogue.
-enum Mode { kFwd = 0, kDz = 1, kDh = 2, kLogits = 3, kGreedy = 4, kDw = 5 };
+// kDzT: the transpose of kDz's output, dZ^T[v][t] = g[t] exp(z[t, v] - lse[t]),
+// from z^T = W h^T (rows = vocabulary, columns = canonical tokens, both
+// operands K-major).  kDwK: kDw with A = dZ^T read K-major.
+enum Mode { kFwd = 0, kDz = 1, kDh = 2, kLogits = 3, kGreedy = 4, kDw = 5, kDzT = 6, kDwK = 7 };
 
 // full / tmem_empty / drain are used in the even CTA only; empty and
 // tmem_full in both (the MMA commits are multicast to the pair).
@@ -111,6 +114,7 @@ struct TileArgs {
     const int32_t *dw_val;   // sorted canonical token indices
     const int32_t *dw_begin, *dw_end;  // [V] range of each target
     float *dw;               // [V, H] output
+    int64_t ntok;            // kDzT: number of canonical token positions (columns)
     // kDz
     const float *lse;   // [T] (global)
     const float *grad;  // [T] (global)
@@ -133,7 +137,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 template <int MODE>
 __device__ __forceinline__ void tile_coords(int64_t tile, const TileArgs &a, int &mb, int &nb) {
-    if constexpr (MODE == kDh || MODE == kDw) {
+    if constexpr (MODE == kDh || MODE == kDw || MODE == kDwK) {
         // groups of kGroupNDh H tiles; inside a group, row blocks outer: CTAs
         // running together share A (dZ rows) and walk W's K (vocabulary) rows
         // in step
@@ -161,7 +165,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       const TileArgs a) {
     // kDh: B is W read as [K = vocabulary rows, N = H columns] (N contiguous,
     // "MN-major"), staged as two 64-column boxes of BK rows per CTA.
-    constexpr bool kBmn = (MODE == kDh || MODE == kDw);
+    constexpr bool kBmn = (MODE == kDh || MODE == kDw || MODE == kDwK);
     constexpr bool kAmn = (MODE == kDw);
     constexpr uint32_t kIdesc = idesc_bf16_f32(2 * BM, BN, kAmn, kBmn);
     constexpr uint32_t kBBoxBytes = BK * 64 * 2;  // one 64-column MN-major box
@@ -479,7 +483,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_bar);
-            } else if constexpr (MODE == kDw) {
+            } else if constexpr (MODE == kDzT) {
+                // rows = vocabulary v, columns = canonical tokens; each column
+                // brings its own lse and g (tokens past the active count have g = 0)
+                const bool vrow = lrow < a.V;
+                const int tvalid = (int)(a.ntok - n0 < (int64_t)BN ? a.ntok - n0 : (int64_t)BN);
+                if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
+                tc_fence_after();
+                const uint32_t taddr = tmem + lane_off + (uint32_t)(b * BN);
+                uint16_t *drow = a.dz + lrow * a.ldz + n0;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
+                    tmem_ld_wait();
+                    const int c0 = c * 32;
+                    if (vrow && c0 < tvalid) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int t0 = n0 + c0 + 2 * j;
+                            const bool ok0 = c0 + 2 * j < tvalid, ok1 = c0 + 2 * j + 1 < tvalid;
+                            const float nl0 = ok0 ? __fmul_rn(-a.lse[t0], kLog2e) : 0.f;
+                            const float nl1 = ok1 ? __fmul_rn(-a.lse[t0 + 1], kLog2e) : 0.f;
+                            const float g0 = ok0 ? a.grad[t0] : 0.f;
+                            const float g1 = ok1 ? a.grad[t0 + 1] : 0.f;
+                            const float p0 = ex2(__fmaf_rn(__uint_as_float(r[2 * j]), kLog2e, nl0));
+                            const float p1 = ex2(__fmaf_rn(__uint_as_float(r[2 * j + 1]), kLog2e, nl1));
+                            pk[j] = pack_bf16x2(__fmul_rn(g0, p0), __fmul_rn(g1, p1));
+                        }
+                        if (c0 + 32 <= tvalid) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(drow + c0);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (c0 + j < tvalid)
+                                    drow[c0 + j] = (uint16_t)((j & 1) ? (pk[j >> 1] >> 16) : (pk[j >> 1] & 0xFFFFu));
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(empty_bar);
+            } else if constexpr (MODE == kDw || MODE == kDwK) {
                 // lrow is a vocabulary row; its one-hot term runs over the
                 // canonical tokens whose target it is, in canonical order
                 const bool vrow = lrow < a.V;
@@ -875,7 +924,8 @@ size_t linear_dw_workspace_bytes(int64_t n, int64_t H, int64_t V) {
     b += 2 * round256(ln * 4) + round256(ln * 8);           // gc, lsec, tgtc
     b += 4 * round256(ln * 4);                              // sort buffers
     b += 2 * round256((size_t)V * 4);                       // begin, end
-    b += round256(ln * (size_t)ld_dz(V) * 2);               // dZ
+    // dZ [n][round_up(V, 8)] or dZ^T [V][round_up(n, 8)], whichever is larger
+    b += round256(std::max(ln * (size_t)ld_dz(V), (size_t)V * (size_t)ld_dz(n)) * 2);
     return b;
 }
 
@@ -943,14 +993,66 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     bf.begin = reinterpret_cast<int32_t *>(take((size_t)V * 4));
     bf.end = reinterpret_cast<int32_t *>(take((size_t)V * 4));
     bf.ldz = ld_dz(V);
-    bf.dz = reinterpret_cast<uint16_t *>(take(ln * (size_t)bf.ldz * 2));
+    bf.dz = reinterpret_cast<uint16_t *>(
+        take(std::max(ln * (size_t)bf.ldz, (size_t)V * (size_t)ld_dz(n)) * 2));
 
     cudaError_t e = launch_dw_prep(h, targets, cu, num_seqs, T, H, V, lse, grad, order, n, bf, di, st);
     if (e != cudaSuccess) return e;
 
+    CUtensorMap tmHc, tmW, tmDzT, tmHcT;
+    const int bits = [&] { int b = 1; while ((int64_t(1) << b) < V) ++b; return b; }();
+    if (!dh) {
+        // dW alone: dZ^T over the canonical tokens (z^T = W h^T, both operands
+        // K-major), then dW with A = dZ^T read K-major
+        const int64_t ldn = ld_dz(n);
+        CUtensorMap tmWa, tmHcb, tmDzTk;
+        if (!encode_tmap_bf16_2d(&tmWa, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BM, true))
+            return cudaErrorInvalidValue;
+        if (!encode_tmap_bf16_2d(&tmHcb, bf.hc, (uint64_t)H, (uint64_t)n, (uint64_t)H * 2, BK,
+                                 BN / 2, true))
+            return cudaErrorInvalidValue;
+        TileArgs t{};
+        t.targets = nullptr;
+        t.rows = V;
+        t.V = (int32_t)V;
+        t.H = (int32_t)H;
+        t.err = di.err;
+        t.lse = bf.lsec;
+        t.grad = bf.gc;
+        t.dz = bf.dz;
+        t.ldz = ldn;
+        t.ntok = n;
+        t.num_m = (int32_t)((V + 2 * BM - 1) / (2 * BM));
+        t.num_n = (int32_t)((n + BN - 1) / BN);
+        t.num_k = (int32_t)(H / BK);
+        e = run_tiles<kDzT>(tmWa, tmHcb, t, di, st);
+        if (e != cudaSuccess) return e;
+        if (!encode_tmap_bf16_2d(&tmDzTk, bf.dz, (uint64_t)n, (uint64_t)V, (uint64_t)ldn * 2, BK, BM,
+                                 true))
+            return cudaErrorInvalidValue;
+        if (!encode_tmap_bf16_2d(&tmHcT, bf.hc, (uint64_t)H, (uint64_t)n, (uint64_t)H * 2, 64, BK,
+                                 true))
+            return cudaErrorInvalidValue;
+        TileArgs d{};
+        d.targets = nullptr;
+        d.rows = V;
+        d.V = (int32_t)V;
+        d.H = (int32_t)H;
+        d.err = di.err;
+        d.hc = bf.hc;
+        d.gc = bf.gc;
+        d.dw_val = (bits % 2 == 0) ? bf.val0 : bf.val1;
+        d.dw_begin = bf.begin;
+        d.dw_end = bf.end;
+        d.dw = dW;
+        d.num_m = (int32_t)((V + 2 * BM - 1) / (2 * BM));
+        d.num_n = (int32_t)((H + BN - 1) / BN);
+        d.num_k = (int32_t)((n + BK - 1) / BK);
+        return run_tiles<kDwK>(tmDzTk, tmHcT, d, di, st);
+    }
+
     // dZ over the canonical tokens (every position past the active count has
     // target -1 and so gives a zero row)
-    CUtensorMap tmHc, tmW, tmDzT, tmHcT;
     if (!encode_tmap_bf16_2d(&tmHc, bf.hc, (uint64_t)H, (uint64_t)n, (uint64_t)H * 2, BK, BM, true))
         return cudaErrorInvalidValue;
     if (!encode_tmap_bf16_2d(&tmW, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2, true))
@@ -1009,7 +1111,6 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     d.err = di.err;
     d.hc = bf.hc;
     d.gc = bf.gc;
-    const int bits = [&] { int b = 1; while ((int64_t(1) << b) < V) ++b; return b; }();
     d.dw_val = (bits % 2 == 0) ? bf.val0 : bf.val1;
     d.dw_begin = bf.begin;
     d.dw_end = bf.end;
