@@ -340,6 +340,9 @@ def measure_rows(rk, pool, zs, peaks, dev, stream) -> dict:
                              "frac": tf / peaks["bf16_tflops_sustained"],
                              "algorithmic": "4*T*H*V flop (dZ recompute + dZ^T h)"}
     # the whole backward (dh + dW) from one shared softmax pass, 6*T*H*V flop
+    del wsd
+    wsd = torch.empty(rk.linear_logp_bwd_full_workspace_size(T, H, V), dtype=torch.uint8,
+                      device=dev)
     dh = torch.empty((T, H), dtype=torch.float32, device=dev)
     ms = time_loop(lambda i: rk.linear_logp_bwd_full(h, W, tg, lse, g, dh=dh, dW=dW, workspace=wsd,
                                                      stream=stream), 3, stream)
@@ -647,6 +650,13 @@ def run_case(args) -> None:
             dW = torch.empty((V, H), dtype=torch.float32, device=dev)
             fn = lambda: rk.linear_logp_dw(h, W, tg, lse, g, dW=dW, workspace=ws)
             flops = 4.0 * T * H * V
+        elif args.case == "full":
+            ws = torch.empty(rk.linear_logp_bwd_full_workspace_size(T, H, V), dtype=torch.uint8,
+                             device=dev)
+            dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+            dh = torch.empty((T, H), dtype=torch.float32, device=dev)
+            fn = lambda: rk.linear_logp_bwd_full(h, W, tg, lse, g, dh=dh, dW=dW, workspace=ws)
+            flops = 6.0 * T * H * V
         else:
             ws = torch.empty(rk.linear_logp_bwd_workspace_size(T, H, V), dtype=torch.uint8,
                              device=dev)
@@ -679,7 +689,7 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the separate timing of the widened rows")
-    ap.add_argument("--case", choices=["fwd", "bwd", "logits", "dw"], default=None)
+    ap.add_argument("--case", choices=["fwd", "bwd", "logits", "dw", "full"], default=None)
     ap.add_argument("--shape", default="2048,4096,32000")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()

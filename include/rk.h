@@ -247,8 +247,10 @@ rk_status rk_linear_logp_dw(const uint16_t *h, const uint16_t *W, const int64_t 
  * row; rows outside the canonical set get 0, active rows with targets >= V
  * get NaN and RK_DEVERR_TARGET_RANGE.
  *   arguments: as rk_linear_logp_dw, plus dh fp32 [T, H] (16-byte aligned);
- *   workspace >= rk_linear_logp_dw_workspace_size(n, H, V) bytes.
+ *   workspace >= rk_linear_logp_bwd_full_workspace_size(n, H, V) bytes (it
+ *   holds g * softmax both as [n, V] for dh and as [V, n] for dW).
  */
+size_t rk_linear_logp_bwd_full_workspace_size(int64_t n, int64_t H, int64_t V);
 rk_status rk_linear_logp_bwd_full(const uint16_t *h, const uint16_t *W, const int64_t *targets,
                                   const int32_t *cu_seqlens, int32_t num_seqs,
                                   int64_t T, int64_t H, int64_t V,

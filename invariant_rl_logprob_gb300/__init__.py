@@ -29,7 +29,7 @@ __all__ = [
     "linear_logp_bwd", "linear_logp_bwd_workspace_size", "linear_logp_bwd_min_workspace_size",
     "lm_head", "logp_from_logits_bwd", "grpo_token_loss", "linear_greedy",
     "linear_greedy_workspace_size", "linear_logp_dw", "linear_logp_dw_workspace_size",
-    "linear_logp_bwd_full",
+    "linear_logp_bwd_full", "linear_logp_bwd_full_workspace_size",
     "get_device_error", "selftest_wait_timeout", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT",
 ]
 
@@ -97,6 +97,8 @@ def load_library() -> ctypes.CDLL:
     lib.rk_linear_logp_dw.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, i64, vp, vp,
                                       sz, vp]
     lib.rk_linear_logp_dw.restype = ctypes.c_int
+    lib.rk_linear_logp_bwd_full_workspace_size.argtypes = [i64, i64, i64]
+    lib.rk_linear_logp_bwd_full_workspace_size.restype = sz
     lib.rk_linear_logp_bwd_full.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, i64,
                                             vp, vp, vp, sz, vp]
     lib.rk_linear_logp_bwd_full.restype = ctypes.c_int
@@ -374,6 +376,10 @@ def linear_logp_dw(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, lse:
     return dW
 
 
+def linear_logp_bwd_full_workspace_size(n: int, H: int, V: int) -> int:
+    return int(load_library().rk_linear_logp_bwd_full_workspace_size(n, H, V))
+
+
 def linear_logp_bwd_full(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor,
                          lse: torch.Tensor, grad_logp: torch.Tensor,
                          cu_seqlens: torch.Tensor | None = None, *,
@@ -400,7 +406,7 @@ def linear_logp_bwd_full(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor
     if dW is None:
         dW = torch.empty((V, H), dtype=torch.float32, device=h.device)
     if workspace is None:
-        need = int(lib.rk_linear_logp_dw_workspace_size(n, H, V))
+        need = int(lib.rk_linear_logp_bwd_full_workspace_size(n, H, V))
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
     st = lib.rk_linear_logp_bwd_full(_ptr(h), _ptr(W), _ptr(targets), _ptr(cu), ns, T, H, V,
                                      _ptr(lse), _ptr(grad_logp), _ptr(row_order), n, _ptr(dh),

@@ -9,17 +9,22 @@
 // put the active tokens into that order once:
 //
 //   compact  the caller's canonical row order (or rows 0..T-1) filtered to
-//            the active rows, order kept (one block, chunked prefix sums);
+//            the active rows, order kept (block counts, one scan of the
+//            counts, then each block writes its rows at its offset);
 //   gather   h, g, lse and the target of every canonical token into dense
 //            buffers; positions past the active count hold zeros and target
 //            -1, so a GEMM over all n positions adds exact zeros for them;
 //   sort     (target, canonical index) pairs by target with a stable
-//            one-bit LSD radix sort (one block): ties keep canonical order;
+//            least-significant-digit radix sort, kRadixBits per pass: a
+//            digit histogram per tile, one scan of the histograms (digit
+//            major, tile minor), then a stable scatter per tile; ties keep
+//            canonical order;
 //   bounds   the [begin, end) range of each target in the sorted list.
 //
 // Every step is deterministic: counts and prefix sums over integers, no
 // floating-point atomics.
 #include <algorithm>
+#include <utility>
 
 #include "rk_device.cuh"
 #include "rk_internal.h"
@@ -28,6 +33,7 @@ namespace rk {
 namespace {
 
 constexpr int kScanThreads = 1024;
+constexpr int kRadixBits = 5;
 
 // Exclusive prefix sum of one int per thread across the block; returns the
 // prefix and writes the block total to *total.
@@ -71,23 +77,56 @@ __device__ __forceinline__ bool candidate_active(const int64_t *order, int64_t i
     return row_active(r, t, cu, num_seqs) && t < V;
 }
 
-// crow[c] = physical row of canonical token c (c < n_active); *n_active.
+// Exclusive prefix sums over cnt[0..len) in place (one block); *total gets
+// the sum when total is not null.
 __global__ void __launch_bounds__(kScanThreads)
-    dw_compact(const int64_t *__restrict__ order, int64_t n, int64_t T,
-               const int64_t *__restrict__ targets, const int32_t *__restrict__ cu, int num_seqs,
-               int64_t V, int64_t *__restrict__ crow, int64_t *__restrict__ n_active) {
-    const int64_t per = (n + kScanThreads - 1) / kScanThreads;
+    scan_counts(int32_t *__restrict__ cnt, int64_t len, int64_t *__restrict__ total) {
+    const int64_t per = (len + kScanThreads - 1) / kScanThreads;
     const int64_t b = (int64_t)threadIdx.x * per;
-    const int64_t e = min(n, b + per);
-    int64_t cnt = 0;
-    for (int64_t i = b; i < e; ++i)
-        cnt += candidate_active(order, i, T, targets, cu, num_seqs, V) ? 1 : 0;
-    int64_t total;
-    int64_t pos = block_exclusive_scan(cnt, &total);
-    for (int64_t i = b; i < e; ++i)
-        if (candidate_active(order, i, T, targets, cu, num_seqs, V))
-            crow[pos++] = candidate_row(order, i);
-    if (threadIdx.x == 0) *n_active = total;
+    const int64_t e = min(len, b + per);
+    int64_t s = 0;
+    for (int64_t i = b; i < e; ++i) s += cnt[i];
+    int64_t all;
+    int64_t pos = block_exclusive_scan(s, &all);
+    for (int64_t i = b; i < e; ++i) {
+        const int32_t c = cnt[i];
+        cnt[i] = (int32_t)pos;
+        pos += c;
+    }
+    if (total && threadIdx.x == 0) *total = all;
+}
+
+// Compaction, first half: the number of active candidates in each block of
+// kScanThreads candidates.
+__global__ void __launch_bounds__(kScanThreads)
+    dw_compact_count(const int64_t *__restrict__ order, int64_t n, int64_t T,
+                     const int64_t *__restrict__ targets, const int32_t *__restrict__ cu,
+                     int num_seqs, int64_t V, int32_t *__restrict__ block_cnt) {
+    const int64_t i = (int64_t)blockIdx.x * kScanThreads + threadIdx.x;
+    const bool a = i < n && candidate_active(order, i, T, targets, cu, num_seqs, V);
+    const int c = __syncthreads_count(a);
+    if (threadIdx.x == 0) block_cnt[blockIdx.x] = c;
+}
+
+// Compaction, second half: crow[offset of the block + rank in the block] =
+// physical row, ranks in candidate order.
+__global__ void __launch_bounds__(kScanThreads)
+    dw_compact_write(const int64_t *__restrict__ order, int64_t n, int64_t T,
+                     const int64_t *__restrict__ targets, const int32_t *__restrict__ cu,
+                     int num_seqs, int64_t V, const int32_t *__restrict__ block_ofs,
+                     int64_t *__restrict__ crow) {
+    __shared__ int warp_cnt[kScanThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t i = (int64_t)blockIdx.x * kScanThreads + threadIdx.x;
+    const bool a = i < n && candidate_active(order, i, T, targets, cu, num_seqs, V);
+    const unsigned m = __ballot_sync(0xffffffffu, a);
+    if (lane == 0) warp_cnt[warp] = __popc(m);
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += warp_cnt[w];
+    if (a)
+        crow[(int64_t)block_ofs[blockIdx.x] + before + __popc(m & ((1u << lane) - 1u))] =
+            candidate_row(order, i);
 }
 
 // Canonical buffers: hc [n, H] bf16, gc / lsec fp32 [n], tgtc int64 [n],
@@ -117,41 +156,87 @@ __global__ void dw_gather(const uint16_t *__restrict__ h, const float *__restric
     }
 }
 
-// Stable LSD radix sort of (key, val) over the first *n_active entries, one
-// bit per pass, keys < 2^bits.  Result in (key0, val0) when bits is even,
-// (key1, val1) when odd.
-__global__ void __launch_bounds__(kScanThreads)
-    dw_radix_sort(int32_t *__restrict__ key0, int32_t *__restrict__ val0,
-                  int32_t *__restrict__ key1, int32_t *__restrict__ val1,
-                  const int64_t *__restrict__ n_active, int bits) {
+constexpr int kSortThreads = 256;
+constexpr int kSortItems = 16;                         // consecutive items per thread
+constexpr int kSortTile = kSortThreads * kSortItems;  // items per block
+constexpr int kBins = 1 << kRadixBits;
+
+// Radix pass, first half: hist[d * tiles + b] = number of items of tile b
+// whose digit (key >> shift) & (kBins - 1) is d.
+__global__ void __launch_bounds__(kSortThreads)
+    radix_histogram(const int32_t *__restrict__ key, const int64_t *__restrict__ n_active,
+                    int shift, int32_t *__restrict__ hist, int tiles) {
+    __shared__ int cnt[kBins];
+    if (threadIdx.x < kBins) cnt[threadIdx.x] = 0;
+    __syncthreads();
     const int64_t n = *n_active;
-    const int64_t per = (n + kScanThreads - 1) / kScanThreads;
-    const int64_t b = (int64_t)threadIdx.x * per;
-    const int64_t e = min(n, b + per);
-    int32_t *ks = key0, *vs = val0, *kd = key1, *vd = val1;
-    for (int bit = 0; bit < bits; ++bit) {
-        int64_t zeros = 0;
-        for (int64_t i = b; i < e; ++i) zeros += ((ks[i] >> bit) & 1) ? 0 : 1;
-        int64_t total_zeros;
-        const int64_t zpos0 = block_exclusive_scan(zeros, &total_zeros);
-        int64_t zpos = zpos0;
-        int64_t opos = total_zeros + (b - zpos0);  // ones before this chunk = b - zeros before
-        for (int64_t i = b; i < e; ++i) {
-            const int32_t k = ks[i];
-            if ((k >> bit) & 1) {
-                kd[opos] = k;
-                vd[opos] = vs[i];
-                ++opos;
-            } else {
-                kd[zpos] = k;
-                vd[zpos] = vs[i];
-                ++zpos;
-            }
-        }
+    const int64_t base = (int64_t)blockIdx.x * kSortTile + (int64_t)threadIdx.x * kSortItems;
+#pragma unroll
+    for (int k = 0; k < kSortItems; ++k)
+        if (base + k < n) atomicAdd(&cnt[(key[base + k] >> shift) & (kBins - 1)], 1);
+    __syncthreads();
+    if (threadIdx.x < kBins) hist[threadIdx.x * tiles + blockIdx.x] = cnt[threadIdx.x];
+}
+
+// Radix pass, second half (after the histograms are scanned): every item goes
+// to hist[d * tiles + b] + (items of digit d earlier in the tile).  A thread's
+// items are consecutive, so "earlier" = in an earlier thread, or earlier in
+// the same thread: the scatter is stable.
+__global__ void __launch_bounds__(kSortThreads)
+    radix_scatter(const int32_t *__restrict__ ks, const int32_t *__restrict__ vs,
+                  int32_t *__restrict__ kd, int32_t *__restrict__ vd,
+                  const int64_t *__restrict__ n_active, int shift,
+                  const int32_t *__restrict__ hist, int tiles) {
+    __shared__ int S[kBins * kSortThreads];  // [digit][thread] counts, then offsets
+    __shared__ int tile_base[kBins];
+    __shared__ int part[kSortThreads];
+    const int t = threadIdx.x;
+    const int64_t n = *n_active;
+    const int64_t base = (int64_t)blockIdx.x * kSortTile + (int64_t)t * kSortItems;
+    int32_t k[kSortItems], v[kSortItems];
+#pragma unroll
+    for (int d = 0; d < kBins; ++d) S[d * kSortThreads + t] = 0;
+#pragma unroll
+    for (int i = 0; i < kSortItems; ++i) {
+        const bool live = base + i < n;
+        k[i] = live ? ks[base + i] : 0;
+        v[i] = live ? vs[base + i] : 0;
+        if (live) ++S[((k[i] >> shift) & (kBins - 1)) * kSortThreads + t];
+    }
+    __syncthreads();
+    // exclusive scan of S in (digit, thread) order: kBins entries per thread
+    constexpr int kPer = kBins * kSortThreads / kSortThreads;
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) sum += S[t * kPer + j];
+    part[t] = sum;
+    __syncthreads();
+    // Hillis-Steele inclusive scan of the per-thread sums
+    for (int off = 1; off < kSortThreads; off <<= 1) {
+        const int y = (t >= off) ? part[t - off] : 0;
         __syncthreads();
-        int32_t *t;
-        t = ks; ks = kd; kd = t;
-        t = vs; vs = vd; vd = t;
+        part[t] += y;
+        __syncthreads();
+    }
+    int run = part[t] - sum;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int c = S[t * kPer + j];
+        S[t * kPer + j] = run;
+        run += c;
+    }
+    __syncthreads();
+    if (t < kBins) tile_base[t] = S[t * kSortThreads];
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kSortItems; ++i) {
+        if (base + i < n) {
+            const int d = (k[i] >> shift) & (kBins - 1);
+            const int64_t pos =
+                (int64_t)hist[d * tiles + blockIdx.x] + (S[d * kSortThreads + t]++ - tile_base[d]);
+            kd[pos] = k[i];
+            vd[pos] = v[i];
+        }
     }
 }
 
@@ -169,24 +254,49 @@ __global__ void dw_bounds(const int32_t *__restrict__ key, const int64_t *__rest
 
 }  // namespace
 
+int64_t dw_scan_entries(int64_t n) {
+    const int64_t blocks = (n + kScanThreads - 1) / kScanThreads;
+    const int64_t tiles = (n + kSortTile - 1) / kSortTile;
+    return std::max<int64_t>(1, std::max(blocks, tiles * (int64_t)kBins));
+}
+
+int dw_sort_passes(int64_t V) {
+    int bits = 1;
+    while ((int64_t(1) << bits) < V) ++bits;
+    return (bits + kRadixBits - 1) / kRadixBits;
+}
+
 cudaError_t launch_dw_prep(const uint16_t *h, const int64_t *targets, const int32_t *cu,
                            int num_seqs, int64_t T, int64_t H, int64_t V, const float *lse,
                            const float *grad, const int64_t *order, int64_t n, const DwBuffers &b,
                            const DeviceInfo &di, cudaStream_t st) {
-    dw_compact<<<1, kScanThreads, 0, st>>>(order, n, T, targets, cu, num_seqs, V, b.crow,
-                                           b.n_active);
+    const unsigned cblocks = (unsigned)((n + kScanThreads - 1) / kScanThreads);
+    dw_compact_count<<<cblocks, kScanThreads, 0, st>>>(order, n, T, targets, cu, num_seqs, V,
+                                                       b.scan);
+    scan_counts<<<1, kScanThreads, 0, st>>>(b.scan, cblocks, b.n_active);
+    dw_compact_write<<<cblocks, kScanThreads, 0, st>>>(order, n, T, targets, cu, num_seqs, V,
+                                                       b.scan, b.crow);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dw_gather<<<(unsigned)n, 128, 0, st>>>(h, grad, lse, targets, b.crow, b.n_active, n, H, b.hc,
                                            b.gc, b.lsec, b.tgtc, b.key0, b.val0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    int bits = 1;
-    while ((int64_t(1) << bits) < V) ++bits;
-    dw_radix_sort<<<1, kScanThreads, 0, st>>>(b.key0, b.val0, b.key1, b.val1, b.n_active, bits);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int32_t *sorted_key = (bits % 2 == 0) ? b.key0 : b.key1;
+    const int passes = dw_sort_passes(V);
+    const int tiles = (int)((n + kSortTile - 1) / kSortTile);
+    int32_t *ks = b.key0, *vs = b.val0, *kd = b.key1, *vd = b.val1;
+    for (int p = 0; p < passes; ++p) {
+        const int shift = p * kRadixBits;
+        radix_histogram<<<tiles, kSortThreads, 0, st>>>(ks, b.n_active, shift, b.scan, tiles);
+        scan_counts<<<1, kScanThreads, 0, st>>>(b.scan, (int64_t)tiles * kBins, nullptr);
+        radix_scatter<<<tiles, kSortThreads, 0, st>>>(ks, vs, kd, vd, b.n_active, shift, b.scan,
+                                                      tiles);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        std::swap(ks, kd);
+        std::swap(vs, vd);
+    }
+    const int32_t *sorted_key = ks;
     e = cudaMemsetAsync(b.begin, 0, (size_t)V * sizeof(int32_t), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(b.end, 0, (size_t)V * sizeof(int32_t), st);
     if (e != cudaSuccess) return e;

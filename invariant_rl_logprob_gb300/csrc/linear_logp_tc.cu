@@ -30,11 +30,13 @@
 //   kFwd  the row's softmax partial over the tile's 256 vocabulary columns,
 //         m = max z, s = sum 2^((z - m) log2 e), and z[target] if the target
 //         is in the tile, written to workspace[row][tile];
-//   kDz   dZ = g exp(z - lse) rounded to bf16 (0 on inactive rows);
+//   kDz   dZ = g exp(z - lse) rounded to bf16 (0 on inactive rows), and,
+//         for the fused full backward, dZ^T as well through TMA stores;
 //   kDh   dh = g W[target] - acc in fp32 (0 on inactive rows);
 //   kLogits  z rounded to bf16 (the dense path's lm_head);
 //   kGreedy  kFwd plus the lowest column holding the tile maximum;
-//   kDw   dW[v, :] = sum over canonical tokens with target v (in canonical
+//   kDzT  kDz's output transposed, from z^T = W h^T;
+//   kDwK  dW[v, :] = sum over canonical tokens with target v (in canonical
 //         order, fp32) of g h  -  (dZ^T h)[v, :].
 // A second small kernel (linear_logp_merge) folds the forward partials of a
 // row in a fixed order into lse and logp.
@@ -47,6 +49,7 @@
 // schedule, or on how the backward cuts T into chunks.  V is never split
 // across CTAs in the backward's sum (no split-K) and no atomics touch results.
 #include <algorithm>
+#include <cstring>
 
 #include "rk_device.cuh"
 #include "rk_internal.h"
@@ -73,12 +76,12 @@ constexpr int kGroupNDh = 16;  // raster group (in H tiles) of the dh GEMM
 // kFwd: forward partials; kDz: backward GEMM 1; kDh: backward GEMM 2;
 // kLogits: the dense path's lm_head (z stored as bf16); kGreedy: kFwd plus
 // each tile's argmax column (greedy decoding).
-// kDw: the weight gradient, dW = S - dZ^T h over canonical tokens (A = dZ and
-// B = h both read MN-major), S the one-hot term added in the epilogue.
 // kDzT: the transpose of kDz's output, dZ^T[v][t] = g[t] exp(z[t, v] - lse[t]),
 // from z^T = W h^T (rows = vocabulary, columns = canonical tokens, both
-// operands K-major).  kDwK: kDw with A = dZ^T read K-major.
-enum Mode { kFwd = 0, kDz = 1, kDh = 2, kLogits = 3, kGreedy = 4, kDw = 5, kDzT = 6, kDwK = 7 };
+// operands K-major).  kDwK: the weight gradient, dW = S - dZ^T h over
+// canonical tokens (A = dZ^T read K-major, B = h read MN-major), S the
+// one-hot term added in the epilogue.
+enum Mode { kFwd = 0, kDz = 1, kDh = 2, kLogits = 3, kGreedy = 4, kDzT = 6, kDwK = 7 };
 
 // full / tmem_empty / drain are used in the even CTA only; empty and
 // tmem_full in both (the MMA commits are multicast to the pair).
@@ -92,7 +95,12 @@ struct Ctl {
     int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(Ctl);
+// kDz with a transposed copy: each epilogue warp stages 32 x 32 bf16 blocks
+// (two buffers) for TMA stores of dZ^T.
+constexpr int kStageT = 32 * 32;  // elements per staging buffer
+constexpr size_t kCtlBytes = (sizeof(Ctl) + 127) / 128 * 128;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kCtlBytes +
+                              (size_t)(kEpiThreads / 32) * 2 * kStageT * 2;
 
 struct TileArgs {
     // row masking (global row index t = row0 + local row)
@@ -108,7 +116,7 @@ struct TileArgs {
     float2 *part;  // [rows][num_n]
     float *ztgt;   // [rows]
     int32_t *pidx; // kGreedy: [rows][num_n] column of each tile's maximum
-    // kDw (rows = vocabulary, columns = H, K = canonical tokens)
+    // kDwK (rows = vocabulary, columns = H, K = canonical tokens)
     const uint16_t *hc;      // [n, H] canonical h
     const float *gc;         // [n] canonical g
     const int32_t *dw_val;   // sorted canonical token indices
@@ -123,6 +131,7 @@ struct TileArgs {
     // kDh
     const uint16_t *W;  // [V][H]
     float *dh;          // [T][H] (global)
+    bool dzT_store;     // kDz: also store dZ^T through the third tensor map
     const int64_t *out_rows;  // kDh over canonical rows: physical row of each (or null)
     int32_t H;
 };
@@ -137,7 +146,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 template <int MODE>
 __device__ __forceinline__ void tile_coords(int64_t tile, const TileArgs &a, int &mb, int &nb) {
-    if constexpr (MODE == kDh || MODE == kDw || MODE == kDwK) {
+    if constexpr (MODE == kDh || MODE == kDwK) {
         // groups of kGroupNDh H tiles; inside a group, row blocks outer: CTAs
         // running together share A (dZ rows) and walk W's K (vocabulary) rows
         // in step
@@ -162,12 +171,11 @@ __device__ __forceinline__ void tile_coords(int64_t tile, const TileArgs &a, int
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     linear_logp_tiles(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const TileArgs a) {
+                      const __grid_constant__ CUtensorMap tmC, const TileArgs a) {
     // kDh: B is W read as [K = vocabulary rows, N = H columns] (N contiguous,
     // "MN-major"), staged as two 64-column boxes of BK rows per CTA.
-    constexpr bool kBmn = (MODE == kDh || MODE == kDw || MODE == kDwK);
-    constexpr bool kAmn = (MODE == kDw);
-    constexpr uint32_t kIdesc = idesc_bf16_f32(2 * BM, BN, kAmn, kBmn);
+    constexpr bool kBmn = (MODE == kDh || MODE == kDwK);
+    constexpr uint32_t kIdesc = idesc_bf16_f32(2 * BM, BN, false, kBmn);
     constexpr uint32_t kBBoxBytes = BK * 64 * 2;  // one 64-column MN-major box
     // Descriptor strides.  K-major, 128B swizzle: 8-row groups 1024 B apart;
     // the next 16-wide K slice starts 32 B further.  MN-major, 128B swizzle:
@@ -175,13 +183,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // apart (stride offset); the next 16-row K slice starts 16*128 B further.
     constexpr uint32_t kBLbo = kBmn ? kBBoxBytes : 16;
     constexpr uint32_t kBStepK = kBmn ? (UK * 128) : (UK * 2);
-    constexpr uint32_t kALbo = kAmn ? kBBoxBytes : 16;
-    constexpr uint32_t kAStepK = kAmn ? (UK * 128) : (UK * 2);
+    constexpr uint32_t kALbo = 16;        // A is always K-major
+    constexpr uint32_t kAStepK = UK * 2;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)kStages * kStageBytes);
+    uint16_t *stageT = reinterpret_cast<uint16_t *>(smem + (size_t)kStages * kStageBytes + kCtlBytes);
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -235,15 +244,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int arow = mb * 2 * BM + (int)rank * BM;     // this CTA's A rows
                 const int bn0 = nb * BN + (int)rank * (BN / 2);    // this CTA's B rows / H columns
                 int nbox0 = 0, nbox1 = 0;    // B boxes of CTA 0 / 1 (MN-major)
-                int abox0 = 1, abox1 = 1;    // A boxes of CTA 0 / 1 (MN-major: up to 2)
                 if constexpr (kBmn) {
                     nbox0 = max(0, min(2, (a.H - nb * BN) / 64));
                     nbox1 = max(0, min(2, (a.H - nb * BN - BN / 2) / 64));
-                }
-                if constexpr (kAmn) {
-                    const int v0 = mb * 2 * BM;
-                    abox0 = max(0, min(2, (a.V - v0 + 63) / 64));
-                    abox1 = max(0, min(2, (a.V - v0 - BM + 63) / 64));
                 }
                 for (int kb = 0; kb < a.num_k; ++kb) {
                     if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort, a.err)) {
@@ -254,21 +257,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t sa = sbase + (uint32_t)(s * kStageBytes);
                     if (rank == 0) {
                         uint32_t bytes = (uint32_t)(2 * kStageBytes);
-                        if constexpr (kAmn)
-                            bytes = (uint32_t)((abox0 + abox1 + nbox0 + nbox1) * (int)kBBoxBytes);
-                        else if constexpr (kBmn)
+                        if constexpr (kBmn)
                             bytes = (uint32_t)(2 * kABytes + (nbox0 + nbox1) * (int)kBBoxBytes);
                         mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), bytes);
                     }
-                    if constexpr (kAmn) {
-                        const int abox = rank == 0 ? abox0 : abox1;
-                        for (int j = 0; j < abox; ++j)
-                            tma_load_2d_pair(sa + j * kBBoxBytes, &tmA, fb, arow + j * 64, kb * BK);
-                        const int nbox = rank == 0 ? nbox0 : nbox1;
-                        for (int j = 0; j < nbox; ++j)
-                            tma_load_2d_pair(sa + kABytes + j * kBBoxBytes, &tmB, fb, bn0 + j * 64,
-                                             kb * BK);
-                    } else if constexpr (kBmn) {
+                    if constexpr (kBmn) {
                         tma_load_2d_pair(sa, &tmA, fb, kb * BK, arow);
                         const int nbox = rank == 0 ? nbox0 : nbox1;
                         for (int j = 0; j < nbox; ++j)
@@ -346,6 +339,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // Epilogue: warp w reads TMEM lanes [32w, 32w+32) = rows of this CTA's half.
         int b = 0;
         uint32_t tph = 0;
+        uint32_t tchunks = 0;  // transposed blocks stored by this warp so far
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         for (int64_t tile = pair; tile < total; tile += npairs) {
             int mb, nb;
@@ -465,6 +459,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                         pk[j] = pack_bf16x2(d0, d1);
                     }
+                    if constexpr (kSoft) {
+                        if (a.dzT_store) {
+                            // dZ^T[n0 + c*32 + j][token]: stage the warp's 32 x 32
+                            // block transposed, then one TMA store (clipped at V
+                            // and at the token count)
+                            uint16_t *sb = stageT + (warp * 2 + (int)(tchunks & 1)) * kStageT;
+                            if (lane == 0 && tchunks >= 2) bulk_wait_group_read<1>();
+                            __syncwarp();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                sb[j * 32 + lane] =
+                                    (uint16_t)((j & 1) ? (pk[j >> 1] >> 16) : (pk[j >> 1] & 0xFFFFu));
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                const int64_t tok0 = (int64_t)mb * 2 * BM + (int64_t)rank * BM + warp * 32;
+                                tma_store_2d(&tmC, smem_u32(sb), (int32_t)tok0, n0 + c * 32);
+                                bulk_commit_group();
+                            }
+                            ++tchunks;
+                        }
+                    }
                     if (in_range) {
                         const int c0 = c * 32;
                         if (c0 + 32 <= valid) {
@@ -528,7 +544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_bar);
-            } else if constexpr (MODE == kDw || MODE == kDwK) {
+            } else if constexpr (MODE == kDwK) {
                 // lrow is a vocabulary row; its one-hot term runs over the
                 // canonical tokens whose target it is, in canonical order
                 const bool vrow = lrow < a.V;
@@ -633,6 +649,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     }
 
+    if constexpr (MODE == kDz) {
+        // transposed blocks must be read out of shared memory and written
+        if (warp < kEpiThreads / 32 && lane == 0 && a.dzT_store) bulk_wait_group_all();
+    }
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // the pair is done with its shared memory and TMEM
@@ -794,18 +814,21 @@ int64_t resident_pairs(const DeviceInfo &di) {
 
 template <int MODE>
 cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const TileArgs &a,
-                      const DeviceInfo &di, cudaStream_t st) {
+                      const DeviceInfo &di, cudaStream_t st, const CUtensorMap *tmC = nullptr) {
     cudaError_t e = set_smem_attr<MODE>(di);
     if (e != cudaSuccess) return e;
     const int64_t tiles = (int64_t)a.num_m * a.num_n;
     if (tiles == 0) return cudaSuccess;
     const int64_t pairs = std::min<int64_t>(tiles, resident_pairs<MODE>(di));
     const unsigned grid = (unsigned)(2 * pairs);
-    linear_logp_tiles<MODE><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, a);
+    CUtensorMap unused;
+    std::memset(&unused, 0, sizeof(unused));
+    linear_logp_tiles<MODE><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, tmC ? *tmC : unused, a);
     return cudaGetLastError();
 }
 
 int64_t ld_dz(int64_t V) { return (V + 7) / 8 * 8; }  // 16-byte aligned dZ rows
+int64_t ld_dzt(int64_t n) { return ld_dz(n); }         // dZ^T rows (tokens)
 
 }  // namespace
 
@@ -924,9 +947,16 @@ size_t linear_dw_workspace_bytes(int64_t n, int64_t H, int64_t V) {
     b += 2 * round256(ln * 4) + round256(ln * 8);           // gc, lsec, tgtc
     b += 4 * round256(ln * 4);                              // sort buffers
     b += 2 * round256((size_t)V * 4);                       // begin, end
+    b += round256((size_t)dw_scan_entries(n) * 4);          // scan counts
     // dZ [n][round_up(V, 8)] or dZ^T [V][round_up(n, 8)], whichever is larger
-    b += round256(std::max(ln * (size_t)ld_dz(V), (size_t)V * (size_t)ld_dz(n)) * 2);
+    b += round256(std::max(ln * (size_t)ld_dz(V), (size_t)V * (size_t)ld_dzt(n)) * 2);
     return b;
+}
+
+size_t linear_bwd_full_workspace_bytes(int64_t n, int64_t H, int64_t V) {
+    if (n <= 0) return 0;
+    // the dW buffers plus a dZ^T [V][round_up(n, 8)] next to dZ
+    return linear_dw_workspace_bytes(n, H, V) + round256((size_t)V * (size_t)ld_dzt(n) * 2);
 }
 
 // Canonical backward: prep + dZ over the canonical tokens, then (if dh) the
@@ -992,20 +1022,50 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     bf.val1 = reinterpret_cast<int32_t *>(take(ln * 4));
     bf.begin = reinterpret_cast<int32_t *>(take((size_t)V * 4));
     bf.end = reinterpret_cast<int32_t *>(take((size_t)V * 4));
+    bf.scan = reinterpret_cast<int32_t *>(take((size_t)dw_scan_entries(n) * 4));
     bf.ldz = ld_dz(V);
     bf.dz = reinterpret_cast<uint16_t *>(
-        take(std::max(ln * (size_t)bf.ldz, (size_t)V * (size_t)ld_dz(n)) * 2));
+        take(std::max(ln * (size_t)bf.ldz, (size_t)V * (size_t)ld_dzt(n)) * 2));
+    // the full backward keeps both dZ (for dh) and dZ^T (for dW)
+    uint16_t *dzT = dh ? reinterpret_cast<uint16_t *>(take((size_t)V * (size_t)ld_dzt(n) * 2)) : bf.dz;
+    const int64_t ldn = ld_dzt(n);
 
     cudaError_t e = launch_dw_prep(h, targets, cu, num_seqs, T, H, V, lse, grad, order, n, bf, di, st);
     if (e != cudaSuccess) return e;
 
-    CUtensorMap tmHc, tmW, tmDzT, tmHcT;
-    const int bits = [&] { int b = 1; while ((int64_t(1) << b) < V) ++b; return b; }();
+    CUtensorMap tmHc, tmW;
+    const bool sorted_in_0 = dw_sort_passes(V) % 2 == 0;
+    // dW = S - dZ^T h with A = dZ^T read K-major (rows = vocabulary, columns =
+    // H, K = canonical tokens), B = h read MN-major
+    auto run_dw = [&]() -> cudaError_t {
+        CUtensorMap tmDzTk, tmHcT2;
+        if (!encode_tmap_bf16_2d(&tmDzTk, dzT, (uint64_t)n, (uint64_t)V, (uint64_t)ldn * 2, BK, BM,
+                                 true))
+            return cudaErrorInvalidValue;
+        if (!encode_tmap_bf16_2d(&tmHcT2, bf.hc, (uint64_t)H, (uint64_t)n, (uint64_t)H * 2, 64, BK,
+                                 true))
+            return cudaErrorInvalidValue;
+        TileArgs d{};
+        d.targets = nullptr;
+        d.rows = V;
+        d.V = (int32_t)V;
+        d.H = (int32_t)H;
+        d.err = di.err;
+        d.hc = bf.hc;
+        d.gc = bf.gc;
+        d.dw_val = sorted_in_0 ? bf.val0 : bf.val1;
+        d.dw_begin = bf.begin;
+        d.dw_end = bf.end;
+        d.dw = dW;
+        d.num_m = (int32_t)((V + 2 * BM - 1) / (2 * BM));
+        d.num_n = (int32_t)((H + BN - 1) / BN);
+        d.num_k = (int32_t)((n + BK - 1) / BK);
+        return run_tiles<kDwK>(tmDzTk, tmHcT2, d, di, st);
+    };
     if (!dh) {
         // dW alone: dZ^T over the canonical tokens (z^T = W h^T, both operands
-        // K-major), then dW with A = dZ^T read K-major
-        const int64_t ldn = ld_dz(n);
-        CUtensorMap tmWa, tmHcb, tmDzTk;
+        // K-major), then the dW GEMM
+        CUtensorMap tmWa, tmHcb;
         if (!encode_tmap_bf16_2d(&tmWa, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BM, true))
             return cudaErrorInvalidValue;
         if (!encode_tmap_bf16_2d(&tmHcb, bf.hc, (uint64_t)H, (uint64_t)n, (uint64_t)H * 2, BK,
@@ -1027,28 +1087,7 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
         t.num_k = (int32_t)(H / BK);
         e = run_tiles<kDzT>(tmWa, tmHcb, t, di, st);
         if (e != cudaSuccess) return e;
-        if (!encode_tmap_bf16_2d(&tmDzTk, bf.dz, (uint64_t)n, (uint64_t)V, (uint64_t)ldn * 2, BK, BM,
-                                 true))
-            return cudaErrorInvalidValue;
-        if (!encode_tmap_bf16_2d(&tmHcT, bf.hc, (uint64_t)H, (uint64_t)n, (uint64_t)H * 2, 64, BK,
-                                 true))
-            return cudaErrorInvalidValue;
-        TileArgs d{};
-        d.targets = nullptr;
-        d.rows = V;
-        d.V = (int32_t)V;
-        d.H = (int32_t)H;
-        d.err = di.err;
-        d.hc = bf.hc;
-        d.gc = bf.gc;
-        d.dw_val = (bits % 2 == 0) ? bf.val0 : bf.val1;
-        d.dw_begin = bf.begin;
-        d.dw_end = bf.end;
-        d.dw = dW;
-        d.num_m = (int32_t)((V + 2 * BM - 1) / (2 * BM));
-        d.num_n = (int32_t)((H + BN - 1) / BN);
-        d.num_k = (int32_t)((n + BK - 1) / BK);
-        return run_tiles<kDwK>(tmDzTk, tmHcT, d, di, st);
+        return run_dw();
     }
 
     // dZ over the canonical tokens (every position past the active count has
@@ -1073,8 +1112,15 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     a.num_m = (int32_t)((n + 2 * BM - 1) / (2 * BM));
     a.num_n = (int32_t)((V + BN - 1) / BN);
     a.num_k = (int32_t)(H / BK);
-    e = run_tiles<kDz>(tmHc, tmW, a, di, st);
+    // dZ^T as well, through 32 x 32 TMA stores from the epilogue
+    CUtensorMap tmDzTs;
+    if (!encode_tmap_bf16_2d(&tmDzTs, dzT, (uint64_t)n, (uint64_t)V, (uint64_t)ldn * 2, 32, 32,
+                             false))
+        return cudaErrorInvalidValue;
+    a.dzT_store = true;
+    e = run_tiles<kDz>(tmHc, tmW, a, di, st, &tmDzTs);
     if (e != cudaSuccess) return e;
+    a.dzT_store = false;
 
     if (dh) {
         // dh over the canonical rows, K = V ascending, each row stored at its
@@ -1095,30 +1141,7 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
         if (e != cudaSuccess) return e;
     }
     if (!dW) return cudaSuccess;
-
-    // dW = S - dZ^T h: rows = vocabulary, columns = H, K = canonical tokens;
-    // A = dZ read as [K][M], B = h read as [K][N], both in 64x64 boxes
-    if (!encode_tmap_bf16_2d(&tmDzT, bf.dz, (uint64_t)V, (uint64_t)n, (uint64_t)bf.ldz * 2, 64, BK,
-                             true))
-        return cudaErrorInvalidValue;
-    if (!encode_tmap_bf16_2d(&tmHcT, bf.hc, (uint64_t)H, (uint64_t)n, (uint64_t)H * 2, 64, BK, true))
-        return cudaErrorInvalidValue;
-    TileArgs d{};
-    d.targets = nullptr;
-    d.rows = V;
-    d.V = (int32_t)V;
-    d.H = (int32_t)H;
-    d.err = di.err;
-    d.hc = bf.hc;
-    d.gc = bf.gc;
-    d.dw_val = (bits % 2 == 0) ? bf.val0 : bf.val1;
-    d.dw_begin = bf.begin;
-    d.dw_end = bf.end;
-    d.dw = dW;
-    d.num_m = (int32_t)((V + 2 * BM - 1) / (2 * BM));
-    d.num_n = (int32_t)((H + BN - 1) / BN);
-    d.num_k = (int32_t)((n + BK - 1) / BK);
-    return run_tiles<kDw>(tmDzT, tmHcT, d, di, st);
+    return run_dw();
 }
 
 int64_t linear_bwd_chunk_quantum() { return BM; }

@@ -349,6 +349,11 @@ rk_status rk_linear_logp_dw(const uint16_t *h, const uint16_t *W, const int64_t 
     return RK_OK;
 }
 
+size_t rk_linear_logp_bwd_full_workspace_size(int64_t n, int64_t H, int64_t V) {
+    if (n <= 0 || H <= 0 || V <= 0) return 0;
+    return rk::linear_bwd_full_workspace_bytes(n, H, V);
+}
+
 rk_status rk_linear_logp_bwd_full(const uint16_t *h, const uint16_t *W, const int64_t *targets,
                                   const int32_t *cu_seqlens, int32_t num_seqs, int64_t T,
                                   int64_t H, int64_t V, const float *lse, const float *grad_logp,
@@ -368,7 +373,7 @@ rk_status rk_linear_logp_bwd_full(const uint16_t *h, const uint16_t *W, const in
         return RK_ERR_UNSUPPORTED;
     if ((h && !aligned(h, 16)) || !aligned(W, 16) || !aligned(dW, 16) || (dh && !aligned(dh, 16)))
         return RK_ERR_UNSUPPORTED;
-    if (n > 0 && (!workspace || workspace_bytes < rk::linear_dw_workspace_bytes(n, H, V)))
+    if (n > 0 && (!workspace || workspace_bytes < rk::linear_bwd_full_workspace_bytes(n, H, V)))
         return RK_ERR_WORKSPACE;
     if (n > 0 && !aligned(workspace, 16)) return RK_ERR_INVALID_ARG;
     DeviceInfo di;

@@ -72,10 +72,16 @@ struct DwBuffers {
     int64_t *tgtc;      // [n] canonical targets (-1 past n_active)
     int32_t *key0, *val0, *key1, *val1;  // [n] sort buffers
     int32_t *begin, *end;                // [V] each target's range in the sorted list
+    int32_t *scan;      // [dw_scan_entries(n)] block counts and digit histograms
     uint16_t *dz;       // [n, ldz] bf16 canonical g * softmax
     int64_t ldz;
 };
 size_t linear_dw_workspace_bytes(int64_t n, int64_t H, int64_t V);
+int64_t dw_scan_entries(int64_t n);
+// radix passes of the target sort: the sorted list ends in (key0, val0) when
+// even, in (key1, val1) when odd
+int dw_sort_passes(int64_t V);
+size_t linear_bwd_full_workspace_bytes(int64_t n, int64_t H, int64_t V);
 cudaError_t launch_dw_prep(const uint16_t *h, const int64_t *targets, const int32_t *cu,
                            int num_seqs, int64_t T, int64_t H, int64_t V, const float *lse,
                            const float *grad, const int64_t *order, int64_t n, const DwBuffers &b,

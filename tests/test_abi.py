@@ -100,6 +100,12 @@ def test_argument_errors_of_the_widened_rows(lib):
     q.restype = sz
     q.argtypes = [i64, i64, i64]
     assert q(0, 64, 100) == 0 and q(100, 64, 1000) > 100 * 1008 * 2
+    qf = lib.rk_linear_logp_bwd_full_workspace_size
+    qf.restype = sz
+    qf.argtypes = [i64, i64, i64]
+    # the full backward holds dZ^T [V, round_up(n, 8)] bf16 beside the dW buffers
+    assert qf(0, 64, 100) == 0
+    assert qf(100, 64, 1000) >= q(100, 64, 1000) + 1000 * 104 * 2
     gr = lib.rk_linear_greedy
     gr.restype = ctypes.c_int
     gr.argtypes = [vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, sz, vp]
