@@ -67,8 +67,10 @@ typedef enum {
 
 /*
  * Bytes of workspace rk_linear_logp needs for T rows (>= 0).  The layout is
- * private: per-row, per-vocab-tile (max, sum-exp) partials plus the target
- * logit of every row.  Returns 0 if T == 0.
+ * private: per-row, per-vocab-tile (max, sum-exp) partials, the target logit
+ * of every row and the counter from which the tile kernel's CTA pairs take
+ * their tiles.  Returns 0 if T == 0.  Calls running at the same time need
+ * separate workspaces.
  */
 size_t rk_linear_logp_workspace_size(int64_t T, int64_t H, int64_t V);
 
@@ -113,7 +115,8 @@ rk_status rk_logp_from_logits(const uint16_t *logits, const int64_t *targets,
 
 /*
  * Bytes of workspace rk_linear_logp_bwd needs to process all T rows in one
- * pass (one bf16 [T, V] buffer of g * softmax probabilities, rounded up).
+ * pass (one bf16 [T, V] buffer of g * softmax probabilities, rounded up, and
+ * 256 bytes for a tile counter).
  * A smaller workspace (but at least rk_linear_logp_bwd_min_workspace_size)
  * makes the call process the rows in chunks; the results do not change.
  */

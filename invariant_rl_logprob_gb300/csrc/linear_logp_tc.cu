@@ -83,14 +83,25 @@ constexpr int kGroupNDh = 16;  // raster group (in H tiles) of the dh GEMM
 // one-hot term added in the epilogue.
 enum Mode { kFwd = 0, kDz = 1, kDh = 2, kLogits = 3, kGreedy = 4, kDzT = 6, kDwK = 7 };
 
-// full / tmem_empty / drain are used in the even CTA only; empty and
-// tmem_full in both (the MMA commits are multicast to the pair).
+// Tile queue: the even CTA's producer takes each tile number (from a global
+// counter, so that pairs take tiles in the order they become free) and
+// publishes it to both CTAs; every other role of the pair reads it there.
+constexpr int kTQ = 8;
+// readers of a queue slot: the MMA thread and 4 epilogue warps of the even
+// CTA, the producer and 4 epilogue warps of the odd CTA
+constexpr int kTQReaders = 2 * (kEpiThreads / 32) + 2;
+
+// full / tmem_empty / drain / tq_empty are used in the even CTA only; empty,
+// tmem_full and tq_full in both (the MMA commits are multicast to the pair).
 struct Ctl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t drain;
+    uint64_t tq_full[kTQ];
+    uint64_t tq_empty[kTQ];
+    int32_t tq[kTQ];  // tile number, or -1: no more tiles
     uint32_t tmem_base;
     int abort;
 };
@@ -123,6 +134,8 @@ struct TileArgs {
     const int32_t *dw_begin, *dw_end;  // [V] range of each target
     float *dw;               // [V, H] output
     int64_t ntok;            // kDzT: number of canonical token positions (columns)
+    // tile counter (zeroed before the launch); null: static round-robin order
+    unsigned *tile_counter;
     // kDz
     const float *lse;   // [T] (global)
     const float *grad;  // [T] (global)
@@ -209,6 +222,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&ctl->tmem_empty[b]), 2 * (kEpiThreads / 32));
         }
         mbar_init(smem_u32(&ctl->drain), 1);
+        for (int i = 0; i < kTQ; ++i) {
+            mbar_init(smem_u32(&ctl->tq_full[i]), 1);
+            mbar_init(smem_u32(&ctl->tq_empty[i]), kTQReaders);
+        }
         ctl->abort = 0;
         fence_mbar_init();
     }
@@ -238,7 +255,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 last_ph[i] = 0;
             }
             bool ok = true;
-            for (int64_t tile = pair; tile < total && ok; tile += npairs) {
+            int q = 0;
+            uint32_t qph = 0;
+            int64_t next_static = pair;
+            while (ok) {
+                int32_t tv;
+                if (rank == 0) {
+                    // take the next tile and publish it to both CTAs
+                    if (!mbar_wait_cluster(smem_u32(&ctl->tq_empty[q]), qph ^ 1u, abort, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    int64_t t;
+                    if (a.tile_counter) {
+                        t = (int64_t)atomicAdd(a.tile_counter, 1u);
+                    } else {
+                        t = next_static;
+                        next_static += npairs;
+                    }
+                    tv = t < total ? (int32_t)t : -1;
+                    for (uint32_t r = 0; r < 2; ++r) {
+                        st_shared_cluster_u32(mapa_shared(smem_u32(&ctl->tq[q]), r), (uint32_t)tv);
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tq_full[q]), r));
+                    }
+                } else {
+                    if (!mbar_wait_cluster(smem_u32(&ctl->tq_full[q]), qph, abort, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tv = ctl->tq[q];
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tq_empty[q]), 0));
+                }
+                if (++q == kTQ) {
+                    q = 0;
+                    qph ^= 1u;
+                }
+                if (tv < 0) break;
+                const int64_t tile = tv;
                 int mb, nb;
                 tile_coords<MODE>(tile, a, mb, nb);
                 const int arow = mb * 2 * BM + (int)rank * BM;     // this CTA's A rows
@@ -298,7 +351,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int b = 0;
             uint32_t tph = 0;
             bool ok = true;
-            for (int64_t tile = pair; tile < total && ok; tile += npairs) {
+            int q = 0;
+            uint32_t qph = 0;
+            while (ok) {
+                if (!mbar_wait_cluster(smem_u32(&ctl->tq_full[q]), qph, abort, a.err)) break;
+                const int32_t tv = ctl->tq[q];
+                mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tq_empty[q]), 0));
+                if (++q == kTQ) {
+                    q = 0;
+                    qph ^= 1u;
+                }
+                if (tv < 0) break;
                 if (!mbar_wait(smem_u32(&ctl->tmem_empty[b]), tph ^ 1u, abort, a.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(b * BN);
@@ -341,7 +404,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t tph = 0;
         uint32_t tchunks = 0;  // transposed blocks stored by this warp so far
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        for (int64_t tile = pair; tile < total; tile += npairs) {
+        int q = 0;
+        uint32_t qph = 0;
+        for (;;) {
+            // every lane waits, as in warp_wait
+            const bool got = mbar_wait_cluster(smem_u32(&ctl->tq_full[q]), qph, abort, a.err);
+            if (__all_sync(0xffffffffu, got) == 0) break;
+            const int32_t tv = ctl->tq[q];
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tq_empty[q]), 0));
+            if (++q == kTQ) {
+                q = 0;
+                qph ^= 1u;
+            }
+            if (tv < 0) break;
+            const int64_t tile = tv;
             int mb, nb;
             tile_coords<MODE>(tile, a, mb, nb);
             const int64_t lrow = (int64_t)mb * 2 * BM + (int64_t)rank * BM + threadIdx.x;  // local row
@@ -821,6 +898,10 @@ cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tile
     if (tiles == 0) return cudaSuccess;
     const int64_t pairs = std::min<int64_t>(tiles, resident_pairs<MODE>(di));
     const unsigned grid = (unsigned)(2 * pairs);
+    if (a.tile_counter) {
+        e = cudaMemsetAsync(a.tile_counter, 0, sizeof(unsigned), st);
+        if (e != cudaSuccess) return e;
+    }
     CUtensorMap unused;
     std::memset(&unused, 0, sizeof(unused));
     linear_logp_tiles<MODE><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, tmC ? *tmC : unused, a);
@@ -832,10 +913,15 @@ int64_t ld_dzt(int64_t n) { return ld_dz(n); }         // dZ^T rows (tokens)
 
 }  // namespace
 
+// Every launcher with a workspace keeps the tile counter of its tile
+// launches in one 256-byte slot of it.
+constexpr size_t kCounterBytes = 256;
+
 size_t linear_fwd_workspace_bytes(int64_t T, int64_t V) {
     if (T <= 0) return 0;
     const int64_t num_n = (V + BN - 1) / BN;
-    return round256((size_t)T * (size_t)num_n * sizeof(float2)) + round256((size_t)T * sizeof(float));
+    return round256((size_t)T * (size_t)num_n * sizeof(float2)) + round256((size_t)T * sizeof(float)) +
+           kCounterBytes;
 }
 
 cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
@@ -864,6 +950,8 @@ cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_
     a.part = reinterpret_cast<float2 *>(workspace);
     a.ztgt = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) +
                                        round256((size_t)T * (size_t)a.num_n * sizeof(float2)));
+    a.tile_counter = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(workspace) +
+                                                  linear_fwd_workspace_bytes(T, V) - kCounterBytes);
     cudaError_t e = run_tiles<kFwd>(tmA, tmB, a, di, st);
     if (e != cudaSuccess) return e;
 
@@ -907,6 +995,7 @@ cudaError_t launch_linear_greedy(const uint16_t *h, const uint16_t *W, const int
     const size_t fwd_bytes = linear_fwd_workspace_bytes(T, V);
     a.ztgt = reinterpret_cast<float *>(w + round256((size_t)T * (size_t)a.num_n * sizeof(float2)));
     a.pidx = reinterpret_cast<int32_t *>(w + fwd_bytes);
+    a.tile_counter = reinterpret_cast<unsigned *>(w + fwd_bytes - kCounterBytes);
     cudaError_t e = run_tiles<kGreedy>(tmA, tmB, a, di, st);
     if (e != cudaSuccess) return e;
     const unsigned mgrid = (unsigned)((T + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock);
@@ -941,7 +1030,7 @@ cudaError_t launch_lm_head(const uint16_t *h, const uint16_t *W, int64_t T, int6
 size_t linear_dw_workspace_bytes(int64_t n, int64_t H, int64_t V) {
     if (n <= 0) return 0;
     const size_t ln = (size_t)n;
-    size_t b = 0;
+    size_t b = kCounterBytes;                               // tile counter
     b += round256(ln * 8) + round256(8);                    // crow, n_active
     b += round256(ln * (size_t)H * 2);                      // hc
     b += 2 * round256(ln * 4) + round256(ln * 8);           // gc, lsec, tgtc
@@ -1009,6 +1098,7 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
         return p;
     };
     const size_t ln = (size_t)n;
+    unsigned *counter = reinterpret_cast<unsigned *>(take(kCounterBytes));
     DwBuffers bf;
     bf.crow = reinterpret_cast<int64_t *>(take(ln * 8));
     bf.n_active = reinterpret_cast<int64_t *>(take(8));
@@ -1046,6 +1136,7 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
                                  true))
             return cudaErrorInvalidValue;
         TileArgs d{};
+        d.tile_counter = counter;
         d.targets = nullptr;
         d.rows = V;
         d.V = (int32_t)V;
@@ -1072,6 +1163,7 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
                                  BN / 2, true))
             return cudaErrorInvalidValue;
         TileArgs t{};
+        t.tile_counter = counter;
         t.targets = nullptr;
         t.rows = V;
         t.V = (int32_t)V;
@@ -1097,6 +1189,7 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     if (!encode_tmap_bf16_2d(&tmW, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2, true))
         return cudaErrorInvalidValue;
     TileArgs a{};
+    a.tile_counter = counter;
     a.targets = bf.tgtc;
     a.cu = nullptr;
     a.num_seqs = 0;
@@ -1147,7 +1240,7 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
 int64_t linear_bwd_chunk_quantum() { return BM; }
 
 size_t linear_bwd_chunk_bytes(int64_t rows, int64_t V) {
-    return round256((size_t)rows * (size_t)ld_dz(V) * 2);
+    return kCounterBytes + round256((size_t)rows * (size_t)ld_dz(V) * 2);
 }
 
 cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
@@ -1157,10 +1250,13 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
     if (T == 0) return cudaSuccess;
     const int64_t ldz = ld_dz(V);
     // rows per chunk: as many whole 128-row blocks as the workspace holds
-    int64_t chunk = (int64_t)(workspace_bytes / ((size_t)ldz * 2)) / BM * BM;
+    // after the tile counter
+    if (workspace_bytes < kCounterBytes) return cudaErrorInvalidValue;
+    int64_t chunk = (int64_t)((workspace_bytes - kCounterBytes) / ((size_t)ldz * 2)) / BM * BM;
     if (chunk <= 0) return cudaErrorInvalidValue;
     if (chunk > T) chunk = T;
-    uint16_t *dz = reinterpret_cast<uint16_t *>(workspace);
+    unsigned *counter = reinterpret_cast<unsigned *>(workspace);
+    uint16_t *dz = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(workspace) + kCounterBytes);
 
     CUtensorMap tmW_k, tmW_mn;
     if (!encode_tmap_bf16_2d(&tmW_k, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2, true))
@@ -1179,6 +1275,7 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
             return cudaErrorInvalidValue;
 
         TileArgs a{};
+        a.tile_counter = counter;
         a.targets = targets;
         a.cu = cu;
         a.num_seqs = num_seqs;

@@ -111,15 +111,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with acquire at cluster scope: for phases completed by arrivals
+// (release.cluster) from the other CTA of the pair, whose shared-memory
+// writes the waiter then reads.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_try_wait_scoped(uint32_t bar, uint32_t parity) {
+    if constexpr (kCluster)
+        return mbar_try_wait_cluster(bar, parity);
+    else
+        return mbar_try_wait(bar, parity);
+}
+
 // Waits until the phase of `bar` with the given parity has completed.
 // Bounded: returns false (after raising *abort and the device error word) if
 // the wait exceeds kWaitLimitNs or another role of the block already aborted.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, volatile int *abort,
                                                 unsigned *err, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_scoped<kCluster>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_scoped<kCluster>(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort) return false;
             if (global_timer_ns() - t0 > limit_ns) {
@@ -133,7 +157,12 @@ __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, v
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           unsigned *err) {
-    return mbar_wait_limit(bar, parity, abort, err, kWaitLimitNs);
+    return mbar_wait_limit<false>(bar, parity, abort, err, kWaitLimitNs);
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort, unsigned *err) {
+    return mbar_wait_limit<true>(bar, parity, abort, err, kWaitLimitNs);
 }
 
 // Same, without the abort protocol: used only for short drains on the abort path.
@@ -267,6 +296,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
+}
+
+// 32-bit store to shared memory of any CTA of the cluster (cluster address).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // Arrive on an mbarrier that may live in another CTA of the cluster.

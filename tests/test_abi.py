@@ -50,13 +50,14 @@ def test_host_only_calls(lib):
     f = lib.rk_linear_logp_workspace_size
     f.restype = ctypes.c_size_t
     f.argtypes = [ctypes.c_int64] * 3
-    # T rows x ceil(V/256) tiles x 8 bytes + T x 4 bytes, each rounded to 256
-    assert f(8192, 4096, 128256) == 8192 * 501 * 8 + 8192 * 4
+    # T rows x ceil(V/256) tiles x 8 bytes + T x 4 bytes, each rounded to 256,
+    # + 256 bytes for the tile counter
+    assert f(8192, 4096, 128256) == 8192 * 501 * 8 + 8192 * 4 + 256
     assert f(0, 4096, 128256) == 0
     g = lib.rk_linear_logp_bwd_workspace_size
     g.restype = ctypes.c_size_t
     g.argtypes = [ctypes.c_int64] * 3
-    assert g(100, 64, 1001) == 128 * 1008 * 2
+    assert g(100, 64, 1001) == 256 + 128 * 1008 * 2
 
 
 def test_argument_errors_return_before_any_launch(lib):
