@@ -64,7 +64,6 @@ constexpr int UK = 16;   // K per tcgen05.mma of kind::f16
 constexpr int kStages = 6;
 constexpr int kABytes = BM * BK * 2;
 constexpr int kBBytes = (BN / 2) * BK * 2;
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * BN;
 constexpr int kEpiThreads = 128;
 constexpr int kProducerWarp = 4;
@@ -110,8 +109,22 @@ struct Ctl {
 // (two buffers) for TMA stores of dZ^T.
 constexpr int kStageT = 32 * 32;  // elements per staging buffer
 constexpr size_t kCtlBytes = (sizeof(Ctl) + 127) / 128 * 128;
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kCtlBytes +
-                              (size_t)(kEpiThreads / 32) * 2 * kStageT * 2;
+constexpr size_t kStageTBytes = (size_t)(kEpiThreads / 32) * 2 * kStageT * 2;
+
+// Per-mode tile shape.  The dh and dW GEMMs take two row blocks per tile: both
+// accumulate into the pair's TMEM at once (columns [0, 256) and [256, 512)),
+// so each B stage (the W or h slice, shared across row blocks) is loaded once
+// for 2 x 256 rows.  That halves how often the long B stream is read, at the
+// cost of the accumulator double buffer (the epilogue is < 1 % of such a tile).
+template <int MODE>
+struct TileCfg {
+    static constexpr int kMB = (MODE == 2 /* kDh */ || MODE == 7 /* kDwK */) ? 2 : 1;
+    static constexpr int kStg = (kMB == 2) ? 4 : kStages;
+    static constexpr int kStgBytes = kMB * kABytes + kBBytes;
+    static constexpr size_t kSmem = 1024 + (size_t)kStg * kStgBytes + kCtlBytes + kStageTBytes;
+    static_assert(kStg <= kStages, "stage barriers");
+    static_assert(kSmem <= 227 * 1024, "shared memory");
+};
 
 struct TileArgs {
     // row masking (global row index t = row0 + local row)
@@ -162,8 +175,9 @@ __device__ __forceinline__ void tile_coords(int64_t tile, const TileArgs &a, int
     if constexpr (MODE == kDh || MODE == kDwK) {
         // groups of kGroupNDh H tiles; inside a group, row blocks outer: CTAs
         // running together share A (dZ rows) and walk W's K (vocabulary) rows
-        // in step
-        const int64_t per_group = (int64_t)a.num_m * kGroupNDh;
+        // in step.  mb counts tiles of TileCfg::kMB row blocks.
+        const int64_t nm = (a.num_m + TileCfg<MODE>::kMB - 1) / TileCfg<MODE>::kMB;
+        const int64_t per_group = nm * kGroupNDh;
         const int64_t g = tile / per_group;
         const int64_t r = tile - g * per_group;
         const int n0 = (int)g * kGroupNDh;
@@ -198,19 +212,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr uint32_t kBStepK = kBmn ? (UK * 128) : (UK * 2);
     constexpr uint32_t kALbo = 16;        // A is always K-major
     constexpr uint32_t kAStepK = UK * 2;
+    constexpr int kMB = TileCfg<MODE>::kMB;
+    constexpr int kStg = TileCfg<MODE>::kStg;
+    constexpr int kStgBytes = TileCfg<MODE>::kStgBytes;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)kStages * kStageBytes);
-    uint16_t *stageT = reinterpret_cast<uint16_t *>(smem + (size_t)kStages * kStageBytes + kCtlBytes);
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)kStg * kStgBytes);
+    uint16_t *stageT = reinterpret_cast<uint16_t *>(smem + (size_t)kStg * kStgBytes + kCtlBytes);
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
     const int64_t pair = blockIdx.x >> 1;
     const int64_t npairs = gridDim.x >> 1;
-    const int64_t total = (int64_t)a.num_m * a.num_n;
+    const int64_t total = (int64_t)((a.num_m + kMB - 1) / kMB) * a.num_n;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -294,7 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int64_t tile = tv;
                 int mb, nb;
                 tile_coords<MODE>(tile, a, mb, nb);
-                const int arow = mb * 2 * BM + (int)rank * BM;     // this CTA's A rows
+                const int arow = mb * kMB * 2 * BM + (int)rank * BM;  // this CTA's A rows
                 const int bn0 = nb * BN + (int)rank * (BN / 2);    // this CTA's B rows / H columns
                 int nbox0 = 0, nbox1 = 0;    // B boxes of CTA 0 / 1 (MN-major)
                 if constexpr (kBmn) {
@@ -307,26 +324,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t fb = mapa_shared(smem_u32(&ctl->full[s]), 0);
-                    const uint32_t sa = sbase + (uint32_t)(s * kStageBytes);
+                    const uint32_t sa = sbase + (uint32_t)(s * kStgBytes);
                     if (rank == 0) {
-                        uint32_t bytes = (uint32_t)(2 * kStageBytes);
+                        uint32_t bytes = (uint32_t)(2 * kStgBytes);
                         if constexpr (kBmn)
-                            bytes = (uint32_t)(2 * kABytes + (nbox0 + nbox1) * (int)kBBoxBytes);
+                            bytes = (uint32_t)(2 * kMB * kABytes + (nbox0 + nbox1) * (int)kBBoxBytes);
                         mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), bytes);
                     }
                     if constexpr (kBmn) {
-                        tma_load_2d_pair(sa, &tmA, fb, kb * BK, arow);
+#pragma unroll
+                        for (int j = 0; j < kMB; ++j)
+                            tma_load_2d_pair(sa + j * kABytes, &tmA, fb, kb * BK, arow + j * 2 * BM);
                         const int nbox = rank == 0 ? nbox0 : nbox1;
                         for (int j = 0; j < nbox; ++j)
-                            tma_load_2d_pair(sa + kABytes + j * kBBoxBytes, &tmB, fb, bn0 + j * 64,
-                                             kb * BK);
+                            tma_load_2d_pair(sa + kMB * kABytes + j * kBBoxBytes, &tmB, fb,
+                                             bn0 + j * 64, kb * BK);
                     } else {
                         tma_load_2d_pair(sa, &tmA, fb, kb * BK, arow);
                         tma_load_2d_pair(sa + kABytes, &tmB, fb, kb * BK, bn0);
                     }
                     used[s] = true;
                     last_ph[s] = ph;
-                    if (++s == kStages) {
+                    if (++s == kStg) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -371,24 +390,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = sbase + (uint32_t)(s * kStageBytes);
-                    const uint64_t ad = smem_desc_sw128(sa, kALbo, 1024);
-                    const uint64_t bd = smem_desc_sw128(sa + kABytes, kBLbo, 1024);
+                    const uint32_t sa = sbase + (uint32_t)(s * kStgBytes);
+                    const uint64_t bd = smem_desc_sw128(sa + kMB * kABytes, kBLbo, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BK / UK; ++kk) {
-                        mma_bf16_ss_pair(d, ad + (uint64_t)((kk * kAStepK) >> 4),
-                                         bd + (uint64_t)((kk * kBStepK) >> 4), kIdesc,
-                                         (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+                        for (int j = 0; j < kMB; ++j) {
+                            const uint64_t ad = smem_desc_sw128(sa + j * kABytes, kALbo, 1024);
+                            mma_bf16_ss_pair(d + (uint32_t)(j * BN), ad + (uint64_t)((kk * kAStepK) >> 4),
+                                             bd + (uint64_t)((kk * kBStepK) >> 4), kIdesc,
+                                             (kb | kk) != 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit_pair(smem_u32(&ctl->empty[s]), 0x3);
-                    if (++s == kStages) {
+                    if (++s == kStg) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (!ok) break;
                 mma_commit_pair(smem_u32(&ctl->tmem_full[b]), 0x3);
-                if (++b == 2) {
+                // two accumulator buffers, or one holding kMB = 2 row blocks
+                if (++b == 2 / kMB) {
                     b = 0;
                     tph ^= 1u;
                 }
@@ -424,7 +447,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int64_t lrow = (int64_t)mb * 2 * BM + (int64_t)rank * BM + threadIdx.x;  // local row
             const bool in_range = lrow < a.rows;
             const int64_t grow = a.row0 + lrow;                    // global row
-            const int64_t tgt = (in_range && a.targets != nullptr) ? a.targets[grow] : -1;
+            const int64_t tgt = (kMB == 1 && in_range && a.targets != nullptr) ? a.targets[grow] : -1;
             const int n0 = nb * BN;
             const uint32_t empty_bar = mapa_shared(smem_u32(&ctl->tmem_empty[b]), 0);
             if constexpr (MODE == kFwd || MODE == kGreedy) {
@@ -622,104 +645,116 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_bar);
             } else if constexpr (MODE == kDwK) {
-                // lrow is a vocabulary row; its one-hot term runs over the
-                // canonical tokens whose target it is, in canonical order
-                const bool vrow = lrow < a.V;
-                const int32_t b0 = vrow ? a.dw_begin[lrow] : 0;
-                const int32_t b1 = vrow ? a.dw_end[lrow] : 0;
-                const int hvalid = min(BN, a.H - n0);
                 if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
                 tc_fence_after();
-                const uint32_t taddr = tmem + lane_off + (uint32_t)(b * BN);
-                float *orow = a.dw + lrow * (int64_t)a.H + n0;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
-                    tmem_ld_wait();
-                    if (vrow && c * 32 < hvalid) {
-                        float sacc[32];
+                for (int j = 0; j < kMB; ++j) {
+                    // vrow is a vocabulary row; its one-hot term runs over the
+                    // canonical tokens whose target it is, in canonical order
+                    const int64_t vr = ((int64_t)mb * kMB + j) * 2 * BM + (int64_t)rank * BM + threadIdx.x;
+                    const bool vrow = vr < a.V;
+                    const int32_t b0 = vrow ? a.dw_begin[vr] : 0;
+                    const int32_t b1 = vrow ? a.dw_end[vr] : 0;
+                    const int hvalid = min(BN, a.H - n0);
+                    const uint32_t taddr = tmem + lane_off + (uint32_t)((b + j) * BN);
+                    float *orow = a.dw + vr * (int64_t)a.H + n0;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
+                        tmem_ld_wait();
+                        if (vrow && c * 32 < hvalid) {
+                            float sacc[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) sacc[j] = 0.f;
-                        for (int32_t i = b0; i < b1; ++i) {
-                            const int32_t tok = a.dw_val[i];
-                            const float w = a.gc[tok];
-                            const uint4 *src =
-                                reinterpret_cast<const uint4 *>(a.hc + (int64_t)tok * a.H + n0 + c * 32);
+                            for (int jj = 0; jj < 32; ++jj) sacc[jj] = 0.f;
+                            for (int32_t i = b0; i < b1; ++i) {
+                                const int32_t tok = a.dw_val[i];
+                                const float w = a.gc[tok];
+                                const uint4 *src = reinterpret_cast<const uint4 *>(
+                                    a.hc + (int64_t)tok * a.H + n0 + c * 32);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const uint4 v4 = __ldg(src + q);
-                                const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+                                for (int qq = 0; qq < 4; ++qq) {
+                                    const uint4 v4 = __ldg(src + qq);
+                                    const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    const int j = q * 8 + u * 2;
-                                    sacc[j] = __fmaf_rn(w, bf16_lo(w4[u]), sacc[j]);
-                                    sacc[j + 1] = __fmaf_rn(w, bf16_hi(w4[u]), sacc[j + 1]);
+                                    for (int u = 0; u < 4; ++u) {
+                                        const int jj = qq * 8 + u * 2;
+                                        sacc[jj] = __fmaf_rn(w, bf16_lo(w4[u]), sacc[jj]);
+                                        sacc[jj + 1] = __fmaf_rn(w, bf16_hi(w4[u]), sacc[jj + 1]);
+                                    }
                                 }
                             }
-                        }
-                        float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
+                            float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(__fsub_rn(sacc[4 * q], __uint_as_float(r[4 * q])),
-                                                 __fsub_rn(sacc[4 * q + 1], __uint_as_float(r[4 * q + 1])),
-                                                 __fsub_rn(sacc[4 * q + 2], __uint_as_float(r[4 * q + 2])),
-                                                 __fsub_rn(sacc[4 * q + 3], __uint_as_float(r[4 * q + 3])));
+                            for (int qq = 0; qq < 8; ++qq)
+                                dst[qq] = make_float4(
+                                    __fsub_rn(sacc[4 * qq], __uint_as_float(r[4 * qq])),
+                                    __fsub_rn(sacc[4 * qq + 1], __uint_as_float(r[4 * qq + 1])),
+                                    __fsub_rn(sacc[4 * qq + 2], __uint_as_float(r[4 * qq + 2])),
+                                    __fsub_rn(sacc[4 * qq + 3], __uint_as_float(r[4 * qq + 3])));
+                        }
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_bar);
             } else {  // kDh
-                const bool active = in_range && row_active(grow, tgt, a.cu, a.num_seqs) && tgt < a.V;
-                const float g = active ? a.grad[grow] : 0.f;
-                const uint16_t *wrow = a.W + (active ? tgt : 0) * (int64_t)a.H + n0;
-                const int hvalid = min(BN, a.H - n0);  // a multiple of 64
-                // canonical rows scatter to their physical rows; padding
-                // positions (inactive) are not stored
-                const bool store = in_range && (a.out_rows == nullptr || active);
-                const int64_t orow_i = (a.out_rows == nullptr) ? grow : (active ? a.out_rows[grow] : 0);
                 if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
                 tc_fence_after();
-                const uint32_t taddr = tmem + lane_off + (uint32_t)(b * BN);
-                float *orow = a.dh + orow_i * (int64_t)a.H + n0;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
-                    tmem_ld_wait();
-                    if (store && c * 32 < hvalid) {
-                        float o[32];
-                        if (active) {
-                            uint4 wv[4];
-                            const uint4 *src = reinterpret_cast<const uint4 *>(wrow + c * 32);
+                for (int j = 0; j < kMB; ++j) {
+                    const int64_t lr = ((int64_t)mb * kMB + j) * 2 * BM + (int64_t)rank * BM + threadIdx.x;
+                    const bool inr = lr < a.rows;
+                    const int64_t gr = a.row0 + lr;
+                    const int64_t tg = inr ? a.targets[gr] : -1;
+                    const bool active = inr && row_active(gr, tg, a.cu, a.num_seqs) && tg < a.V;
+                    const float g = active ? a.grad[gr] : 0.f;
+                    const uint16_t *wrow = a.W + (active ? tg : 0) * (int64_t)a.H + n0;
+                    const int hvalid = min(BN, a.H - n0);  // a multiple of 64
+                    // canonical rows scatter to their physical rows; padding
+                    // positions (inactive) are not stored
+                    const bool store = inr && (a.out_rows == nullptr || active);
+                    const int64_t orow_i = (a.out_rows == nullptr) ? gr : (active ? a.out_rows[gr] : 0);
+                    const uint32_t taddr = tmem + lane_off + (uint32_t)((b + j) * BN);
+                    float *orow = a.dh + orow_i * (int64_t)a.H + n0;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
+                        tmem_ld_wait();
+                        if (store && c * 32 < hvalid) {
+                            float o[32];
+                            if (active) {
+                                uint4 wv[4];
+                                const uint4 *src = reinterpret_cast<const uint4 *>(wrow + c * 32);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) wv[q] = __ldg(src + q);
+                                for (int qq = 0; qq < 4; ++qq) wv[qq] = __ldg(src + qq);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const uint32_t w4[4] = {wv[q].x, wv[q].y, wv[q].z, wv[q].w};
+                                for (int qq = 0; qq < 4; ++qq) {
+                                    const uint32_t w4[4] = {wv[qq].x, wv[qq].y, wv[qq].z, wv[qq].w};
 #pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    const int j = q * 8 + u * 2;
-                                    o[j] = __fmaf_rn(g, bf16_lo(w4[u]), -__uint_as_float(r[j]));
-                                    o[j + 1] = __fmaf_rn(g, bf16_hi(w4[u]), -__uint_as_float(r[j + 1]));
+                                    for (int u = 0; u < 4; ++u) {
+                                        const int jj = qq * 8 + u * 2;
+                                        o[jj] = __fmaf_rn(g, bf16_lo(w4[u]), -__uint_as_float(r[jj]));
+                                        o[jj + 1] = __fmaf_rn(g, bf16_hi(w4[u]), -__uint_as_float(r[jj + 1]));
+                                    }
                                 }
+                            } else {
+#pragma unroll
+                                for (int jj = 0; jj < 32; ++jj) o[jj] = 0.f;
                             }
-                        } else {
+                            float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) o[j] = 0.f;
+                            for (int qq = 0; qq < 8; ++qq)
+                                dst[qq] = make_float4(o[4 * qq], o[4 * qq + 1], o[4 * qq + 2], o[4 * qq + 3]);
                         }
-                        float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_bar);
             }
-            if (++b == 2) {
+            if (++b == 2 / kMB) {
                 b = 0;
                 tph ^= 1u;
             }
@@ -864,7 +899,8 @@ cudaError_t set_smem_attr(const DeviceInfo &di) {
     static thread_local int done_dev = -1;
     if (done_dev == di.device) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(linear_logp_tiles<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)TileCfg<MODE>::kSmem);
     if (e == cudaSuccess) done_dev = di.device;
     return e;
 }
@@ -878,7 +914,7 @@ int64_t resident_pairs(const DeviceInfo &di) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * (di.sm_count / 2)));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = TileCfg<MODE>::kSmem;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, linear_logp_tiles<MODE>, &cfg) != cudaSuccess || n <= 0) {
         (void)cudaGetLastError();
@@ -894,7 +930,8 @@ cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tile
                       const DeviceInfo &di, cudaStream_t st, const CUtensorMap *tmC = nullptr) {
     cudaError_t e = set_smem_attr<MODE>(di);
     if (e != cudaSuccess) return e;
-    const int64_t tiles = (int64_t)a.num_m * a.num_n;
+    const int64_t tiles =
+        (int64_t)((a.num_m + TileCfg<MODE>::kMB - 1) / TileCfg<MODE>::kMB) * a.num_n;
     if (tiles == 0) return cudaSuccess;
     const int64_t pairs = std::min<int64_t>(tiles, resident_pairs<MODE>(di));
     const unsigned grid = (unsigned)(2 * pairs);
@@ -904,7 +941,8 @@ cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tile
     }
     CUtensorMap unused;
     std::memset(&unused, 0, sizeof(unused));
-    linear_logp_tiles<MODE><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, tmC ? *tmC : unused, a);
+    linear_logp_tiles<MODE><<<grid, kThreads, TileCfg<MODE>::kSmem, st>>>(tmA, tmB,
+                                                                        tmC ? *tmC : unused, a);
     return cudaGetLastError();
 }
 
