@@ -214,7 +214,9 @@ def test_tiny_backward_all_rows(rk):
     assert rk.get_device_error() == 0
 
 
-@pytest.mark.parametrize("T,H,V", [(200, 192, 1000), (130, 320, 4097), (3, 64, 9)])
+# (700, ...) gives three 256-row blocks: the dh GEMM's last two-block tile is
+# half outside the rows
+@pytest.mark.parametrize("T,H,V", [(200, 192, 1000), (130, 320, 4097), (3, 64, 9), (700, 128, 2001)])
 def test_backward_shapes(rk, T, H, V):
     gen = synth.generator(2000 + T + H + V)
     W = synth.normal_bf16(gen, (V, H), 0.05)
@@ -241,6 +243,28 @@ def test_backward_chunking_is_invisible(rk):
     wmin = torch.empty(rk.linear_logp_bwd_min_workspace_size(H, V), dtype=torch.uint8, device=DEV)
     chunked = rk.linear_logp_bwd(hd, Wd, tgd, lse, gd, workspace=wmin)
     assert same_bits(full, chunked)
+
+
+def test_workspace_contents_are_ignored(rk):
+    # the workspaces hold the tile counters the launches zero themselves:
+    # garbage in them changes nothing
+    gen = synth.generator(77)
+    T, H, V = 600, 128, 3000
+    W = synth.normal_bf16(gen, (V, H), 0.05)
+    h = synth.normal_bf16(gen, (T, H), 1.0)
+    tg = synth.uniform_targets(gen, T, V)
+    g = torch.randn(T, generator=gen, dtype=torch.float32)
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    lp0, lse0 = rk.linear_logp(hd, Wd, tgd)
+    dh0 = rk.linear_logp_bwd(hd, Wd, tgd, lse0, gd)
+    wf = torch.full((rk.linear_logp_workspace_size(T, H, V),), 0xA5, dtype=torch.uint8, device=DEV)
+    wb = torch.full((rk.linear_logp_bwd_workspace_size(T, H, V),), 0x5A, dtype=torch.uint8,
+                    device=DEV)
+    for _ in range(2):   # the second call finds the first call's counters
+        lp1, lse1 = rk.linear_logp(hd, Wd, tgd, workspace=wf)
+        dh1 = rk.linear_logp_bwd(hd, Wd, tgd, lse1, gd, workspace=wb)
+        assert same_bits(lp1, lp0) and same_bits(lse1, lse0) and same_bits(dh1, dh0)
+    assert rk.get_device_error() == 0
 
 
 def test_backward_masking(rk):
