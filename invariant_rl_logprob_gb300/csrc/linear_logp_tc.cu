@@ -108,8 +108,9 @@ struct Ctl {
 // kDz with a transposed copy: each epilogue warp stages 32 x 32 bf16 blocks
 // (two buffers) for TMA stores of dZ^T.
 constexpr int kStageT = 32 * 32;  // elements per staging buffer
-constexpr size_t kCtlBytes = (sizeof(Ctl) + 127) / 128 * 128;
-constexpr size_t kStageTBytes = (size_t)(kEpiThreads / 32) * 2 * kStageT * 2;
+constexpr size_t kCtlBytes = (sizeof(Ctl) + 1023) / 1024 * 1024;  // staging stays 1024-aligned
+// kDz staging: per epilogue warp two chunk slots of [dZ block, dZ^T block]
+constexpr size_t kStageTBytes = (size_t)(kEpiThreads / 32) * 4 * kStageT * 2;
 
 // Per-mode tile shape.  The dh and dW GEMMs take two row blocks per tile: both
 // accumulate into the pair's TMEM at once (columns [0, 256) and [256, 512)),
@@ -121,7 +122,8 @@ struct TileCfg {
     static constexpr int kMB = (MODE == 2 /* kDh */ || MODE == 7 /* kDwK */) ? 2 : 1;
     static constexpr int kStg = (kMB == 2) ? 4 : kStages;
     static constexpr int kStgBytes = kMB * kABytes + kBBytes;
-    static constexpr size_t kSmem = 1024 + (size_t)kStg * kStgBytes + kCtlBytes + kStageTBytes;
+    static constexpr size_t kSmem =
+        1024 + (size_t)kStg * kStgBytes + kCtlBytes + (MODE == 1 /* kDz */ ? kStageTBytes : 0);
     static_assert(kStg <= kStages, "stage barriers");
     static_assert(kSmem <= 227 * 1024, "shared memory");
 };
@@ -158,6 +160,7 @@ struct TileArgs {
     const uint16_t *W;  // [V][H]
     float *dh;          // [T][H] (global)
     bool dzT_store;     // kDz: also store dZ^T through the third tensor map
+    bool dz_tma;        // kDz: store dZ through the fourth tensor map (else plain stores)
     const int64_t *out_rows;  // kDh over canonical rows: physical row of each (or null)
     int32_t H;
 };
@@ -198,7 +201,8 @@ __device__ __forceinline__ void tile_coords(int64_t tile, const TileArgs &a, int
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     linear_logp_tiles(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmC, const TileArgs a) {
+                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                      const TileArgs a) {
     // kDh: B is W read as [K = vocabulary rows, N = H columns] (N contiguous,
     // "MN-major"), staged as two 64-column boxes of BK rows per CTA.
     constexpr bool kBmn = (MODE == kDh || MODE == kDwK);
@@ -560,28 +564,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         pk[j] = pack_bf16x2(d0, d1);
                     }
                     if constexpr (kSoft) {
-                        if (a.dzT_store) {
-                            // dZ^T[n0 + c*32 + j][token]: stage the warp's 32 x 32
-                            // block transposed, then one TMA store (clipped at V
-                            // and at the token count)
-                            uint16_t *sb = stageT + (warp * 2 + (int)(tchunks & 1)) * kStageT;
+                        if (a.dz_tma || a.dzT_store) {
+                            // The warp's 32 x 32 block goes out through TMA
+                            // stores (clipped at V and at the row count): dZ
+                            // from rows of 64 bytes with the 64-byte swizzle
+                            // (16-byte chunk q of row r at chunk q ^ ((r >> 1) & 3),
+                            // so a quarter-warp's writes hit distinct banks),
+                            // and dZ^T[n0 + c*32 + j][token] transposed.
+                            uint16_t *sbz = stageT + (warp * 4 + (int)(tchunks & 1) * 2) * kStageT;
+                            uint16_t *sbt = sbz + kStageT;
                             if (lane == 0 && tchunks >= 2) bulk_wait_group_read<1>();
                             __syncwarp();
+                            if (a.dz_tma) {
+                                uint8_t *rowp = reinterpret_cast<uint8_t *>(sbz) + lane * 64;
+                                const int sw = (lane >> 1) & 3;
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                sb[j * 32 + lane] =
-                                    (uint16_t)((j & 1) ? (pk[j >> 1] >> 16) : (pk[j >> 1] & 0xFFFFu));
+                                for (int qq = 0; qq < 4; ++qq)
+                                    *reinterpret_cast<uint4 *>(rowp + ((qq ^ sw) << 4)) =
+                                        make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
+                            }
+                            if (a.dzT_store) {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    sbt[j * 32 + lane] =
+                                        (uint16_t)((j & 1) ? (pk[j >> 1] >> 16) : (pk[j >> 1] & 0xFFFFu));
+                            }
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
                                 const int64_t tok0 = (int64_t)mb * 2 * BM + (int64_t)rank * BM + warp * 32;
-                                tma_store_2d(&tmC, smem_u32(sb), (int32_t)tok0, n0 + c * 32);
+                                if (a.dz_tma) tma_store_2d(&tmD, smem_u32(sbz), n0 + c * 32, (int32_t)tok0);
+                                if (a.dzT_store) tma_store_2d(&tmC, smem_u32(sbt), (int32_t)tok0, n0 + c * 32);
                                 bulk_commit_group();
                             }
                             ++tchunks;
                         }
                     }
-                    if (in_range) {
+                    if (in_range && !(kSoft && a.dz_tma)) {
                         const int c0 = c * 32;
                         if (c0 + 32 <= valid) {
                             uint4 *dst = reinterpret_cast<uint4 *>(drow + c0);
@@ -763,7 +782,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if constexpr (MODE == kDz) {
         // transposed blocks must be read out of shared memory and written
-        if (warp < kEpiThreads / 32 && lane == 0 && a.dzT_store) bulk_wait_group_all();
+        if (warp < kEpiThreads / 32 && lane == 0 && (a.dzT_store || a.dz_tma)) bulk_wait_group_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -927,7 +946,8 @@ int64_t resident_pairs(const DeviceInfo &di) {
 
 template <int MODE>
 cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const TileArgs &a,
-                      const DeviceInfo &di, cudaStream_t st, const CUtensorMap *tmC = nullptr) {
+                      const DeviceInfo &di, cudaStream_t st, const CUtensorMap *tmC = nullptr,
+                      const CUtensorMap *tmD = nullptr) {
     cudaError_t e = set_smem_attr<MODE>(di);
     if (e != cudaSuccess) return e;
     const int64_t tiles =
@@ -941,8 +961,8 @@ cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tile
     }
     CUtensorMap unused;
     std::memset(&unused, 0, sizeof(unused));
-    linear_logp_tiles<MODE><<<grid, kThreads, TileCfg<MODE>::kSmem, st>>>(tmA, tmB,
-                                                                        tmC ? *tmC : unused, a);
+    linear_logp_tiles<MODE><<<grid, kThreads, TileCfg<MODE>::kSmem, st>>>(
+        tmA, tmB, tmC ? *tmC : unused, tmD ? *tmD : unused, a);
     return cudaGetLastError();
 }
 
@@ -1248,10 +1268,16 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     if (!encode_tmap_bf16_2d(&tmDzTs, dzT, (uint64_t)n, (uint64_t)V, (uint64_t)ldn * 2, 32, 32,
                              false))
         return cudaErrorInvalidValue;
+    CUtensorMap tmDzS;
+    if (!encode_tmap_bf16_2d_sw64(&tmDzS, bf.dz, (uint64_t)V, (uint64_t)n, (uint64_t)bf.ldz * 2, 32,
+                                  32))
+        return cudaErrorInvalidValue;
     a.dzT_store = true;
-    e = run_tiles<kDz>(tmHc, tmW, a, di, st, &tmDzTs);
+    a.dz_tma = true;
+    e = run_tiles<kDz>(tmHc, tmW, a, di, st, &tmDzTs, &tmDzS);
     if (e != cudaSuccess) return e;
     a.dzT_store = false;
+    a.dz_tma = false;
 
     if (dh) {
         // dh over the canonical rows, K = V ascending, each row stored at its
@@ -1330,11 +1356,17 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
         a.dh = dh;
         a.num_m = (int32_t)((rows + 2 * BM - 1) / (2 * BM));
 
-        // GEMM 1: z recomputed, dZ = g exp(z - lse) in bf16
+        // GEMM 1: z recomputed, dZ = g exp(z - lse) in bf16, stored by TMA
+        CUtensorMap tmDzS;
+        if (!encode_tmap_bf16_2d_sw64(&tmDzS, dz, (uint64_t)V, (uint64_t)rows, (uint64_t)ldz * 2, 32,
+                                      32))
+            return cudaErrorInvalidValue;
         a.num_n = (int32_t)((V + BN - 1) / BN);
         a.num_k = (int32_t)(H / BK);
-        cudaError_t e = run_tiles<kDz>(tmH, tmW_k, a, di, st);
+        a.dz_tma = true;
+        cudaError_t e = run_tiles<kDz>(tmH, tmW_k, a, di, st, nullptr, &tmDzS);
         if (e != cudaSuccess) return e;
+        a.dz_tma = false;
 
         // GEMM 2: dh = g W[target] - dZ W, K = V in one ascending pass
         a.num_n = (int32_t)((H + BN - 1) / BN);

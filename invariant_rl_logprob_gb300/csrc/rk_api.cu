@@ -38,7 +38,7 @@ void load_encode() {
 
 bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, uint32_t esize, const void *base,
                uint64_t inner, uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
-               uint32_t box_outer, bool sw128) {
+               uint32_t box_outer, CUtensorMapSwizzle swizzle) {
     std::call_once(g_encode_once, load_encode);
     if (!g_encode) return false;
     (void)esize;
@@ -48,7 +48,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, uint32_t esize, const v
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -64,7 +64,14 @@ bool encode_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uin
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                          bool sw128) {
     return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, outer,
-                     row_stride_bytes, box_inner, box_outer, sw128);
+                     row_stride_bytes, box_inner, box_outer,
+                     sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+bool encode_tmap_bf16_2d_sw64(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                              uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, outer,
+                     row_stride_bytes, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 void record_cuda_error(int e) { g_last_cuda_error = e; }

@@ -27,6 +27,9 @@ cudaError_t current_device_info(DeviceInfo *di);
 bool encode_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                          bool sw128);
+// The same with 64-byte swizzle (boxes whose rows are at most 64 bytes).
+bool encode_tmap_bf16_2d_sw64(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                              uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 
 // ---- logits path (logits_logp.cu) ----
 cudaError_t launch_logits_logp(const uint16_t *logits, const int64_t *targets, const int32_t *cu,
