@@ -41,6 +41,17 @@ __device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p) {
     return v;
 }
 
+// Programmatic dependent launch.  The logits kernels are launched so that
+// their blocks may become resident while the previous kernel in the stream
+// finishes; each block then waits (griddepcontrol.wait) until that kernel has
+// completed and its writes are visible, before it reads anything.  Right after
+// that wait it lets the next such launch start the same way.  Stream order is
+// therefore unchanged; only launch latency overlaps.
+__device__ __forceinline__ void wait_prior_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Elementwise max of two bf16 pairs (exact).
 __device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
     uint32_t d;
@@ -106,6 +117,7 @@ __global__ void __launch_bounds__(kThreads)
                        const int32_t *__restrict__ cu, int num_seqs, int64_t T, int64_t V,
                        float *__restrict__ logp, float *__restrict__ lse, unsigned *err) {
     __shared__ float sh_m[kThreads / 32], sh_s[kThreads / 32];
+    wait_prior_grid();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int wr = warp % kWarpsPerRow;
@@ -173,6 +185,7 @@ __global__ void __launch_bounds__(kThreads)
                       const int32_t *__restrict__ cu, int num_seqs, int64_t T, int64_t V,
                       const float *__restrict__ lse, const float *__restrict__ grad,
                       float *__restrict__ dlogits, unsigned *err) {
+    wait_prior_grid();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int vl = (warp % kWarpsPerRow) * 32 + lane;
@@ -228,6 +241,21 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Launch configuration with programmatic stream serialisation (see
+// wait_prior_grid).
+void dependent_launch_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, unsigned grid,
+                             cudaStream_t st) {
+    *cfg = cudaLaunchConfig_t{};
+    cfg->gridDim = dim3(grid);
+    cfg->blockDim = dim3(kThreads);
+    cfg->dynamicSmemBytes = 0;
+    cfg->stream = st;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+}
+
 }  // namespace
 
 cudaError_t launch_logits_bwd(const uint16_t *logits, const int64_t *targets, const int32_t *cu,
@@ -238,13 +266,14 @@ cudaError_t launch_logits_bwd(const uint16_t *logits, const int64_t *targets, co
     const unsigned grid = (unsigned)((T + kRowsPerBlock - 1) / kRowsPerBlock);
     const bool vec = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0) &&
                      ((reinterpret_cast<uintptr_t>(dlogits) & 15u) == 0);
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    dependent_launch_config(&cfg, attr, grid, st);
     if (vec)
-        logits_bwd_kernel<true><<<grid, kThreads, 0, st>>>(logits, targets, cu, num_seqs, T, V,
-                                                           lse, grad, dlogits, di.err);
-    else
-        logits_bwd_kernel<false><<<grid, kThreads, 0, st>>>(logits, targets, cu, num_seqs, T, V,
-                                                            lse, grad, dlogits, di.err);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, logits_bwd_kernel<true>, logits, targets, cu, num_seqs, T,
+                                  V, lse, grad, dlogits, di.err);
+    return cudaLaunchKernelEx(&cfg, logits_bwd_kernel<false>, logits, targets, cu, num_seqs, T, V,
+                              lse, grad, dlogits, di.err);
 }
 
 cudaError_t launch_logits_logp(const uint16_t *logits, const int64_t *targets, const int32_t *cu,
@@ -253,13 +282,14 @@ cudaError_t launch_logits_logp(const uint16_t *logits, const int64_t *targets, c
     if (T == 0) return cudaSuccess;
     const unsigned grid = (unsigned)((T + kRowsPerBlock - 1) / kRowsPerBlock);
     const bool vec = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    dependent_launch_config(&cfg, attr, grid, st);
     if (vec)
-        logits_logp_kernel<true><<<grid, kThreads, 0, st>>>(logits, targets, cu, num_seqs, T, V,
-                                                            logp, lse, di.err);
-    else
-        logits_logp_kernel<false><<<grid, kThreads, 0, st>>>(logits, targets, cu, num_seqs, T, V,
-                                                             logp, lse, di.err);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, logits_logp_kernel<true>, logits, targets, cu, num_seqs, T,
+                                  V, logp, lse, di.err);
+    return cudaLaunchKernelEx(&cfg, logits_logp_kernel<false>, logits, targets, cu, num_seqs, T, V,
+                              logp, lse, di.err);
 }
 
 }  // namespace rk
