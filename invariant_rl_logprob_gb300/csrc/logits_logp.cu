@@ -230,9 +230,11 @@ __global__ void __launch_bounds__(kThreads)
             d[j] = live ? __fmul_rn(g, __fsub_rn(oh, p)) : fill;
         }
         if (VEC) {
-            float4 *dst = reinterpret_cast<float4 *>(orow + c0);
-            dst[0] = make_float4(d[0], d[1], d[2], d[3]);
-            dst[1] = make_float4(d[4], d[5], d[6], d[7]);
+            // one 32-byte store per lane: a warp writes 1 KB contiguously
+            asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(orow + c0),
+                         "f"(d[0]), "f"(d[1]), "f"(d[2]), "f"(d[3]), "f"(d[4]), "f"(d[5]), "f"(d[6]),
+                         "f"(d[7])
+                         : "memory");
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -264,8 +266,10 @@ cudaError_t launch_logits_bwd(const uint16_t *logits, const int64_t *targets, co
                               cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const unsigned grid = (unsigned)((T + kRowsPerBlock - 1) / kRowsPerBlock);
+    // VEC: 16-byte loads and 32-byte stores (rows of V % 8 == 0 elements keep
+    // both aligned)
     const bool vec = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0) &&
-                     ((reinterpret_cast<uintptr_t>(dlogits) & 15u) == 0);
+                     ((reinterpret_cast<uintptr_t>(dlogits) & 31u) == 0);
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     dependent_launch_config(&cfg, attr, grid, st);

@@ -111,6 +111,21 @@ def test_logits_bwd_invariance(rk):
     assert same_bits(one[0], base[5])
 
 
+def test_logits_bwd_output_alignment(rk):
+    # an output only 16-byte aligned takes the element-wise store path; the
+    # bits are the same as from the 32-byte store path
+    z, tg, _ = synth.logits_batch(T=64, V=4096, seed=12)
+    g = torch.randn(64, generator=synth.generator(13), dtype=torch.float32)
+    zd, tgd, gd = cuda(z), cuda(tg), cuda(g)
+    _, lse = rk.logp_from_logits(zd, tgd)
+    base = rk.logp_from_logits_bwd(zd, tgd, lse, gd)
+    buf = torch.empty(64 * 4096 + 4, dtype=torch.float32, device=DEV)
+    out = buf[4:].view(64, 4096)
+    assert out.data_ptr() % 32 == 16
+    rk.logp_from_logits_bwd(zd, tgd, lse, gd, out=out)
+    assert same_bits(out, base)
+
+
 # --------------------------------------------------------------------------
 # per-token GRPO loss, and the chain logp -> loss -> dh
 # --------------------------------------------------------------------------
