@@ -245,6 +245,30 @@ def test_backward_chunking_is_invisible(rk):
     assert same_bits(full, chunked)
 
 
+def test_many_short_tiles(rk):
+    # H = 64 gives one K stage per forward / dZ tile, so the producer runs
+    # many tiles ahead of the epilogue and the tile queue wraps many times
+    gen = synth.generator(88)
+    T, H, V = 2048, 64, 20000
+    W = synth.normal_bf16(gen, (V, H), 0.1)
+    h = synth.normal_bf16(gen, (T, H), 1.0)
+    tg = synth.uniform_targets(gen, T, V)
+    g = torch.randn(T, generator=gen, dtype=torch.float32)
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    logp, lse = rk.linear_logp(hd, Wd, tgd)
+    dh = rk.linear_logp_bwd(hd, Wd, tgd, lse, gd)
+    rows = synth.sample_rows(T, 48, seed=3)
+    ref_logp, ref_lse = oracle_linear(bits_np(h), bits_np(W), tg.numpy(), rows=rows)
+    _check_fwd(logp[rows], lse[rows], ref_logp, ref_lse, "H=64 many tiles")
+    ref_dh = oracle_bwd(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy(), rows=rows)
+    _check_bwd(dh[rows], ref_dh, "H=64 many tiles")
+    # and the same rows alone give the same bits
+    sub = torch.as_tensor(rows, device=DEV)
+    lp1, lse1 = rk.linear_logp(hd[sub].contiguous(), Wd, tgd[sub].contiguous())
+    assert same_bits(lp1, logp[sub]) and same_bits(lse1, lse[sub])
+    assert rk.get_device_error() == 0
+
+
 def test_workspace_contents_are_ignored(rk):
     # the workspaces hold the tile counters the launches zero themselves:
     # garbage in them changes nothing
