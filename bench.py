@@ -11,7 +11,7 @@ device time, inputs resident in HBM.  h (512 MB) and W (1.05 GB) exceed the
 126 MB L2, so nothing carries over between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-    python bench.py --case {fwd,bwd,logits,dw} [--shape T,H,V] [--reps R]
+    python bench.py --case {fwd,bwd,dw,full,logits,logits_bwd} [--shape T,H,V] [--reps R]
 
 `--case` runs one operator a few times on a small workload (for profiler
 captures; default T=2048, H=4096, V=32000: W and the logits exceed L2) and
@@ -631,11 +631,18 @@ def run_case(args) -> None:
     rk_build.build()
     dev = torch.device("cuda", 0)
     T, H, V = (int(x) for x in args.shape.split(","))
-    if args.case == "logits":
+    if args.case in ("logits", "logits_bwd"):
         z, tg, _ = synth.logits_batch(T=T, V=V)
         z, tg = z.to(dev), tg.to(dev)
-        fn = lambda: rk.logp_from_logits(z, tg)
-        nbytes = T * V * 2 + T * 16
+        if args.case == "logits":
+            fn = lambda: rk.logp_from_logits(z, tg)
+            nbytes = T * V * 2 + T * 16
+        else:
+            _, lse = rk.logp_from_logits(z, tg)
+            g = torch.randn(T, device=dev)
+            dl = torch.empty((T, V), dtype=torch.float32, device=dev)
+            fn = lambda: rk.logp_from_logits_bwd(z, tg, lse, g, out=dl)
+            nbytes = T * V * 6 + T * 16
         work = f"{nbytes / 1e6:.1f} MB"
     else:
         pool = synth.make_pool(H, V, [T], seed=4, with_grad=True)
@@ -689,7 +696,8 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the separate timing of the widened rows")
-    ap.add_argument("--case", choices=["fwd", "bwd", "logits", "dw", "full"], default=None)
+    ap.add_argument("--case", choices=["fwd", "bwd", "logits", "logits_bwd", "dw", "full"],
+                    default=None)
     ap.add_argument("--shape", default="2048,4096,32000")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
