@@ -80,7 +80,12 @@ constexpr int kGroupNDh = 16;  // raster group (in H tiles) of the dh GEMM
 // operands K-major).  kDwK: the weight gradient, dW = S - dZ^T h over
 // canonical tokens (A = dZ^T read K-major, B = h read MN-major), S the
 // one-hot term added in the epilogue.
-enum Mode { kFwd = 0, kDz = 1, kDh = 2, kLogits = 3, kGreedy = 4, kDzT = 6, kDwK = 7 };
+// kDh2, kDwK2: kDh and kDwK with two row blocks per tile (see TileCfg).
+enum Mode {
+    kFwd = 0, kDz = 1, kDh = 2, kLogits = 3, kGreedy = 4, kDzT = 6, kDwK = 7, kDh2 = 8, kDwK2 = 9
+};
+__host__ __device__ constexpr bool mode_dh(int m) { return m == kDh || m == kDh2; }
+__host__ __device__ constexpr bool mode_dw(int m) { return m == kDwK || m == kDwK2; }
 
 // Tile queue: the even CTA's producer takes each tile number (from a global
 // counter, so that pairs take tiles in the order they become free) and
@@ -112,14 +117,15 @@ constexpr size_t kCtlBytes = (sizeof(Ctl) + 1023) / 1024 * 1024;  // staging sta
 // kDz staging: per epilogue warp two chunk slots of [dZ block, dZ^T block]
 constexpr size_t kStageTBytes = (size_t)(kEpiThreads / 32) * 4 * kStageT * 2;
 
-// Per-mode tile shape.  The dh and dW GEMMs take two row blocks per tile: both
+// Per-mode tile shape.  kDh2 and kDwK2 take two row blocks per tile: both
 // accumulate into the pair's TMEM at once (columns [0, 256) and [256, 512)),
 // so each B stage (the W or h slice, shared across row blocks) is loaded once
 // for 2 x 256 rows.  That halves how often the long B stream is read, at the
-// cost of the accumulator double buffer (the epilogue is < 1 % of such a tile).
+// cost of the accumulator double buffer; the launchers pick them only for
+// long K loops and enough tiles (run_rows).
 template <int MODE>
 struct TileCfg {
-    static constexpr int kMB = (MODE == 2 /* kDh */ || MODE == 7 /* kDwK */) ? 2 : 1;
+    static constexpr int kMB = (MODE == 8 /* kDh2 */ || MODE == 9 /* kDwK2 */) ? 2 : 1;
     static constexpr int kStg = (kMB == 2) ? 4 : kStages;
     static constexpr int kStgBytes = kMB * kABytes + kBBytes;
     static constexpr size_t kSmem =
@@ -175,7 +181,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 template <int MODE>
 __device__ __forceinline__ void tile_coords(int64_t tile, const TileArgs &a, int &mb, int &nb) {
-    if constexpr (MODE == kDh || MODE == kDwK) {
+    if constexpr (mode_dh(MODE) || mode_dw(MODE)) {
         // groups of kGroupNDh H tiles; inside a group, row blocks outer: CTAs
         // running together share A (dZ rows) and walk W's K (vocabulary) rows
         // in step.  mb counts tiles of TileCfg::kMB row blocks.
@@ -205,7 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       const TileArgs a) {
     // kDh: B is W read as [K = vocabulary rows, N = H columns] (N contiguous,
     // "MN-major"), staged as two 64-column boxes of BK rows per CTA.
-    constexpr bool kBmn = (MODE == kDh || MODE == kDwK);
+    constexpr bool kBmn = mode_dh(MODE) || mode_dw(MODE);
     constexpr uint32_t kIdesc = idesc_bf16_f32(2 * BM, BN, false, kBmn);
     constexpr uint32_t kBBoxBytes = BK * 64 * 2;  // one 64-column MN-major box
     // Descriptor strides.  K-major, 128B swizzle: 8-row groups 1024 B apart;
@@ -663,7 +669,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_bar);
-            } else if constexpr (MODE == kDwK) {
+            } else if constexpr (mode_dw(MODE)) {
                 if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
                 tc_fence_after();
 #pragma unroll 1
@@ -717,7 +723,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_bar);
-            } else {  // kDh
+            } else {  // kDh, kDh2
                 if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
                 tc_fence_after();
 #pragma unroll 1
@@ -966,6 +972,19 @@ cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tile
     return cudaGetLastError();
 }
 
+// The dh / dW GEMMs: two row blocks per tile when the K loop is long (the
+// un-overlapped epilogue is then a small part of a tile) and there are enough
+// such tiles for about 8 rounds of the resident pairs; one row block per tile
+// otherwise.  Either way every accumulator sees the same MMA sequence, so the
+// choice does not change any bit.
+template <int M1, int M2>
+cudaError_t run_rows(const CUtensorMap &tmA, const CUtensorMap &tmB, const TileArgs &a,
+                     const DeviceInfo &di, cudaStream_t st) {
+    const int64_t two = (int64_t)((a.num_m + 1) / 2) * a.num_n;
+    if (a.num_k >= 256 && two >= 8 * resident_pairs<M2>(di)) return run_tiles<M2>(tmA, tmB, a, di, st);
+    return run_tiles<M1>(tmA, tmB, a, di, st);
+}
+
 int64_t ld_dz(int64_t V) { return (V + 7) / 8 * 8; }  // 16-byte aligned dZ rows
 int64_t ld_dzt(int64_t n) { return ld_dz(n); }         // dZ^T rows (tokens)
 
@@ -1209,7 +1228,7 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
         d.num_m = (int32_t)((V + 2 * BM - 1) / (2 * BM));
         d.num_n = (int32_t)((H + BN - 1) / BN);
         d.num_k = (int32_t)((n + BK - 1) / BK);
-        return run_tiles<kDwK>(tmDzTk, tmHcT2, d, di, st);
+        return run_rows<kDwK, kDwK2>(tmDzTk, tmHcT2, d, di, st);
     };
     if (!dh) {
         // dW alone: dZ^T over the canonical tokens (z^T = W h^T, both operands
@@ -1294,7 +1313,7 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
         q.out_rows = bf.crow;
         q.num_n = (int32_t)((H + BN - 1) / BN);
         q.num_k = (int32_t)((V + BK - 1) / BK);
-        e = run_tiles<kDh>(tmDz, tmWmn, q, di, st);
+        e = run_rows<kDh, kDh2>(tmDz, tmWmn, q, di, st);
         if (e != cudaSuccess) return e;
     }
     if (!dW) return cudaSuccess;
@@ -1371,7 +1390,7 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
         // GEMM 2: dh = g W[target] - dZ W, K = V in one ascending pass
         a.num_n = (int32_t)((H + BN - 1) / BN);
         a.num_k = (int32_t)((V + BK - 1) / BK);
-        e = run_tiles<kDh>(tmDz, tmW_mn, a, di, st);
+        e = run_rows<kDh, kDh2>(tmDz, tmW_mn, a, di, st);
         if (e != cudaSuccess) return e;
     }
     linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(targets, cu, num_seqs, T, (int32_t)V,

@@ -114,3 +114,26 @@ def test_full_backward_matches_separate_calls(rk):
     ref = oracle.linear_logp_dw(bits_np(lay.h), bits_np(pool.W), np.where(act, tg.numpy(), -100),
                                 np.nan_to_num(lay.g.double().numpy()), lay.cu_seqlens.numpy())
     assert contract.check_gradient_accuracy(dw_full.cpu().numpy(), ref).passed
+
+
+def test_one_and_two_row_blocks_per_tile_agree(rk):
+    # Long K loops with many tiles run the dh and dW GEMMs with two row blocks
+    # per tile; short ones with one.  Each accumulator sees the same MMAs
+    # either way, so the bits must agree.
+    T, H, V = 20480, 4096, 20480
+    h, W, tg, g = _case(T, H, V, 57, w_std=0.02)
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    _, lse = rk.linear_logp(hd, Wd, tgd)
+    # dh: the whole group (two blocks per tile) vs 128-row chunks (one)
+    dh_two = rk.linear_logp_bwd(hd, Wd, tgd, lse, gd)
+    wmin = torch.empty(rk.linear_logp_bwd_min_workspace_size(H, V), dtype=torch.uint8, device=DEV)
+    dh_one = rk.linear_logp_bwd(hd, Wd, tgd, lse, gd, workspace=wmin)
+    assert same_bits(dh_two, dh_one)
+    # dW: 10000 active tokens named alone (K = 10000 tokens, one block per
+    # tile) vs the same tokens among 20480 candidates (two blocks per tile)
+    tg2 = tgd.clone()
+    tg2[10000:] = -100
+    dw_one = rk.linear_logp_dw(hd, Wd, tg2, lse, gd, row_order=torch.arange(10000, device=DEV))
+    dw_two = rk.linear_logp_dw(hd, Wd, tg2, lse, gd)
+    assert same_bits(dw_one, dw_two)
+    assert rk.get_device_error() == 0
