@@ -129,7 +129,8 @@ struct TileCfg {
     static constexpr int kStg = (kMB == 2) ? 4 : kStages;
     static constexpr int kStgBytes = kMB * kABytes + kBBytes;
     static constexpr size_t kSmem =
-        1024 + (size_t)kStg * kStgBytes + kCtlBytes + (MODE == 1 /* kDz */ ? kStageTBytes : 0);
+        1024 + (size_t)kStg * kStgBytes + kCtlBytes +
+        ((MODE == 1 /* kDz */ || MODE == 6 /* kDzT */) ? kStageTBytes : 0);
     static_assert(kStg <= kStages, "stage barriers");
     static_assert(kSmem <= 227 * 1024, "shared memory");
 };
@@ -166,7 +167,8 @@ struct TileArgs {
     const uint16_t *W;  // [V][H]
     float *dh;          // [T][H] (global)
     bool dzT_store;     // kDz: also store dZ^T through the third tensor map
-    bool dz_tma;        // kDz: store dZ through the fourth tensor map (else plain stores)
+    bool dz_tma;        // kDz / kDzT: store the output through the fourth tensor map
+                        // (else plain stores)
     const int64_t *out_rows;  // kDh over canonical rows: physical row of each (or null)
     int32_t H;
 };
@@ -639,7 +641,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
                     tmem_ld_wait();
                     const int c0 = c * 32;
-                    if (vrow && c0 < tvalid) {
+                    if (c0 < tvalid) {  // the same for the whole warp
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
@@ -653,16 +655,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             const float p1 = ex2(__fmaf_rn(__uint_as_float(r[2 * j + 1]), kLog2e, nl1));
                             pk[j] = pack_bf16x2(__fmul_rn(g0, p0), __fmul_rn(g1, p1));
                         }
-                        if (c0 + 32 <= tvalid) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(drow + c0);
+                        if (a.dz_tma) {
+                            // the warp's 32 x 32 block through one TMA store, as
+                            // in kDz (rows past V and tokens past ntok are clipped)
+                            uint16_t *sbz = stageT + (warp * 4 + (int)(tchunks & 1) * 2) * kStageT;
+                            if (lane == 0 && tchunks >= 2) bulk_wait_group_read<1>();
+                            __syncwarp();
+                            uint8_t *rowp = reinterpret_cast<uint8_t *>(sbz) + lane * 64;
+                            const int sw = (lane >> 1) & 3;
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                        } else {
+                            for (int qq = 0; qq < 4; ++qq)
+                                *reinterpret_cast<uint4 *>(rowp + ((qq ^ sw) << 4)) =
+                                    make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                const int64_t v0 = (int64_t)mb * 2 * BM + (int64_t)rank * BM + warp * 32;
+                                tma_store_2d(&tmD, smem_u32(sbz), n0 + c0, (int32_t)v0);
+                                bulk_commit_group();
+                            }
+                            ++tchunks;
+                        } else if (vrow) {
+                            if (c0 + 32 <= tvalid) {
+                                uint4 *dst = reinterpret_cast<uint4 *>(drow + c0);
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (c0 + j < tvalid)
-                                    drow[c0 + j] = (uint16_t)((j & 1) ? (pk[j >> 1] >> 16) : (pk[j >> 1] & 0xFFFFu));
+                                for (int q = 0; q < 4; ++q)
+                                    dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (c0 + j < tvalid)
+                                        drow[c0 + j] = (uint16_t)((j & 1) ? (pk[j >> 1] >> 16) : (pk[j >> 1] & 0xFFFFu));
+                            }
                         }
                     }
                 }
@@ -786,8 +810,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     }
 
-    if constexpr (MODE == kDz) {
-        // transposed blocks must be read out of shared memory and written
+    if constexpr (MODE == kDz || MODE == kDzT) {
+        // staged blocks must be read out of shared memory and written
         if (warp < kEpiThreads / 32 && lane == 0 && (a.dzT_store || a.dz_tma)) bulk_wait_group_all();
     }
     tc_fence_before();
@@ -1254,7 +1278,12 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
         t.num_m = (int32_t)((V + 2 * BM - 1) / (2 * BM));
         t.num_n = (int32_t)((n + BN - 1) / BN);
         t.num_k = (int32_t)(H / BK);
-        e = run_tiles<kDzT>(tmWa, tmHcb, t, di, st);
+        CUtensorMap tmDzTs;
+        if (!encode_tmap_bf16_2d_sw64(&tmDzTs, dzT, (uint64_t)n, (uint64_t)V, (uint64_t)ldn * 2, 32,
+                                      32))
+            return cudaErrorInvalidValue;
+        t.dz_tma = true;
+        e = run_tiles<kDzT>(tmWa, tmHcb, t, di, st, nullptr, &tmDzTs);
         if (e != cudaSuccess) return e;
         return run_dw();
     }
