@@ -52,9 +52,9 @@ WORKLOAD = ("grpo_fwd_bwd: linear_logp fwd+bwd T=65536 (64x1024) H=4096 V=128256
 #  --warmup 3 --no-cpu-baseline --no-rows`, one pass per launch), recorded with
 # the SHA-1 of the kernel source; reported only while the source still matches.
 TRAFFIC_RECORD = {
-    "source_sha1": "f34c51f9cb513b5699e6b641623e6d3f0593e2e6",
-    "bytes_per_step": 190986237696,
-    "per_launch_gb": {"fwd": 18.76, "dZ": 36.59, "dh": 135.64},
+    "source_sha1": "9a6ee361aef166a34fca32898fe987604032f50b",
+    "bytes_per_step": 197629855488,
+    "per_launch_gb": {"fwd": 18.76, "dZ": 36.62, "dh": 142.24},
 }
 # Unique bytes a step has to move: forward h + W + partials; dZ GEMM h + W +
 # dZ written; dh GEMM dZ + W read, dh written.
