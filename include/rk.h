@@ -19,6 +19,10 @@
  *  - All tensor pointers are DEVICE pointers, owned by the caller, contiguous
  *    row-major.  The library never allocates device memory; scratch space is
  *    passed in as `workspace`.  Outputs must not alias inputs or each other.
+ *  - Workspace contents on entry are ignored.  Besides intermediates, every
+ *    workspace holds the counter from which the tile kernel's CTA pairs take
+ *    their tiles (the call zeroes it), so calls that may run at the same time
+ *    (other streams, other host threads) need separate workspaces.
  *  - bf16 tensors are passed as `const uint16_t*` (IEEE bfloat16 bit patterns).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
  *    asynchronous and stream-ordered; none synchronises the host.
