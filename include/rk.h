@@ -68,6 +68,9 @@ typedef enum {
 /* Device error word bits (rk_get_device_error). */
 #define RK_DEVERR_TARGET_RANGE 0x1  /* an active row had target >= V */
 #define RK_DEVERR_TIMEOUT 0x2       /* a pipeline wait gave up after its time limit */
+#define RK_DEVERR_LSE 0x4           /* a backward row had more than 64 columns with
+                                       p >= 1/64: the lse passed in does not belong
+                                       to these inputs (results unspecified) */
 
 /*
  * Bytes of workspace rk_linear_logp needs for T rows (>= 0).  The layout is
@@ -140,8 +143,15 @@ size_t rk_linear_logp_bwd_min_workspace_size(int64_t H, int64_t V);
  *   dh         fp32 [T, H] output
  *   workspace  >= rk_linear_logp_bwd_min_workspace_size(H, V) bytes, 256-byte aligned
  * The sum over v runs in one fixed ascending order for every row (no split of
- * V across blocks, no atomics); the probabilities enter that sum rounded to
- * bf16, the one-hot term is applied in fp32.
+ * V across blocks, no atomic additions of values).  Per row, the target
+ * column and every column with p >= 1/64 (at most 65 columns) are handled in
+ * fp32: w = g (onehot - p), summed over those columns in ascending column
+ * order.  All other probabilities enter a tensor-core sum rounded to bf16,
+ * where each carries at most 1/64 of the row's mass.  So a peaked softmax (a
+ * confident policy, p_target near 1) does not turn dh = g (1 - p_t) (...)
+ * into a small difference of large bf16-rounded terms.  An lse that does not
+ * belong to the inputs can make more than 64 columns qualify: the extra ones
+ * are dropped and RK_DEVERR_LSE is set.
  */
 rk_status rk_linear_logp_bwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
                              const int32_t *cu_seqlens, int32_t num_seqs,
@@ -232,9 +242,11 @@ rk_status rk_linear_greedy(const uint16_t *h, const uint16_t *W, const int32_t *
  *   lse, grad_logp fp32 [T]; dW fp32 [V, H] output (16-byte aligned);
  *   workspace >= rk_linear_logp_dw_workspace_size(n, H, V) bytes, where n is
  *   n_order (or T): canonical copies of h and of g * softmax (bf16 [n, V]).
- * The one-hot term is accumulated in fp32 per vocabulary row over its
- * tokens in canonical order; the softmax term is a tensor-core GEMM with
- * K = the canonical tokens in one ascending pass.
+ * As in rk_linear_logp_bwd, each token's target column and its columns with
+ * p >= 1/64 are handled in fp32: per vocabulary row, the fp32 terms
+ * g (onehot - p) h_i are summed over those tokens in canonical order.  The
+ * remaining g p h_i terms are a tensor-core GEMM with K = the canonical
+ * tokens in one ascending pass.
  */
 size_t rk_linear_logp_dw_workspace_size(int64_t n, int64_t H, int64_t V);
 rk_status rk_linear_logp_dw(const uint16_t *h, const uint16_t *W, const int64_t *targets,

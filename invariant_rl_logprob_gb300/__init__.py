@@ -30,7 +30,7 @@ __all__ = [
     "lm_head", "logp_from_logits_bwd", "grpo_token_loss", "linear_greedy",
     "linear_greedy_workspace_size", "linear_logp_dw", "linear_logp_dw_workspace_size",
     "linear_logp_bwd_full", "linear_logp_bwd_full_workspace_size",
-    "get_device_error", "selftest_wait_timeout", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT",
+    "get_device_error", "selftest_wait_timeout", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT", "DEVERR_LSE",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -40,6 +40,7 @@ _lib = None
 RK_OK, RK_ERR_INVALID_ARG, RK_ERR_UNSUPPORTED, RK_ERR_WORKSPACE, RK_ERR_CUDA = range(5)
 DEVERR_TARGET_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
+DEVERR_LSE = 0x4
 
 
 class RkError(RuntimeError):

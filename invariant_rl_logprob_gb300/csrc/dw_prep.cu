@@ -14,12 +14,16 @@
 //   gather   h, g, lse and the target of every canonical token into dense
 //            buffers; positions past the active count hold zeros and target
 //            -1, so a GEMM over all n positions adds exact zeros for them;
-//   sort     (target, canonical index) pairs by target with a stable
+// After the dZ / dZ^T GEMM over the canonical tokens has filled each token's
+// list of fp32 entries (the target column and the columns with p >= 1/64):
+//   flatten  the lists in canonical token order (per-token counts, one scan);
+//   sort     (column, flat index) pairs by column with a stable
 //            least-significant-digit radix sort, kRadixBits per pass: a
 //            digit histogram per tile, one scan of the histograms (digit
-//            major, tile minor), then a stable scatter per tile; ties keep
-//            canonical order;
-//   bounds   the [begin, end) range of each target in the sorted list.
+//            major, tile minor), then a stable scatter per tile; a column's
+//            entries keep canonical token order;
+//   bounds   the [begin, end) range of each column in the sorted list.
+// A separate kernel sorts each row's own list by column (for the dh GEMM).
 //
 // Every step is deterministic: counts and prefix sums over integers, no
 // floating-point atomics.
@@ -129,14 +133,12 @@ __global__ void __launch_bounds__(kScanThreads)
             candidate_row(order, i);
 }
 
-// Canonical buffers: hc [n, H] bf16, gc / lsec fp32 [n], tgtc int64 [n],
-// key / val int32 [n] (sort input).
+// Canonical buffers: hc [n, H] bf16, gc / lsec fp32 [n], tgtc int64 [n].
 __global__ void dw_gather(const uint16_t *__restrict__ h, const float *__restrict__ grad,
                           const float *__restrict__ lse, const int64_t *__restrict__ targets,
                           const int64_t *__restrict__ crow, const int64_t *__restrict__ n_active,
                           int64_t n, int64_t H, uint16_t *__restrict__ hc, float *__restrict__ gc,
-                          float *__restrict__ lsec, int64_t *__restrict__ tgtc,
-                          int32_t *__restrict__ key, int32_t *__restrict__ val) {
+                          float *__restrict__ lsec, int64_t *__restrict__ tgtc) {
     const int64_t c = blockIdx.x;
     if (c >= n) return;
     const int64_t na = *n_active;
@@ -151,8 +153,6 @@ __global__ void dw_gather(const uint16_t *__restrict__ h, const float *__restric
         lsec[c] = live ? lse[r] : 0.f;
         const int64_t t = live ? targets[r] : -1;
         tgtc[c] = t;
-        key[c] = (int32_t)t;
-        val[c] = (int32_t)c;
     }
 }
 
@@ -240,7 +240,58 @@ __global__ void __launch_bounds__(kSortThreads)
     }
 }
 
-// begin/end (pre-zeroed, [V]) of each target's range in the sorted keys.
+// Each row's entry list sorted by column: entry i goes to the number of
+// entries of the row with a smaller column (the columns of a row are
+// distinct).  One warp per row.
+constexpr int kSortRowsPerBlock = 8;
+__global__ void __launch_bounds__(32 * kSortRowsPerBlock)
+    sort_entries(const int32_t *__restrict__ ecount, int2 *__restrict__ ent, int64_t rows) {
+    __shared__ int2 buf[kSortRowsPerBlock][kEntCap];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * kSortRowsPerBlock + w;
+    if (r >= rows) return;
+    const int c = min(ecount[r], kEntCap);
+    if (c <= 1) return;
+    int2 *row = ent + r * kEntCap;
+    for (int i = lane; i < c; i += 32) buf[w][i] = row[i];
+    __syncwarp();
+    for (int i = lane; i < c; i += 32) {
+        const int2 e = buf[w][i];
+        int pos = 0;
+        for (int j = 0; j < c; ++j) pos += (buf[w][j].x < e.x) ? 1 : 0;
+        row[pos] = e;
+    }
+}
+
+// Per-token entry counts (capped) for the flat list.
+__global__ void entries_count(const int32_t *__restrict__ ecount, int64_t n,
+                              int32_t *__restrict__ eoff) {
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n;
+         t += (int64_t)gridDim.x * blockDim.x)
+        eoff[t] = min(ecount[t], kEntCap);
+}
+
+// The flat list: token t's entries at eoff[t] (exclusive prefix sums), as
+// (column, flat index) sort pairs plus the token and w of each entry.
+__global__ void entries_scatter(const int32_t *__restrict__ eoff, const int2 *__restrict__ ent,
+                                int64_t n, int32_t *__restrict__ key, int32_t *__restrict__ val,
+                                int32_t *__restrict__ ent_t, float *__restrict__ ent_w,
+                                const int32_t *__restrict__ ecount) {
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int c = min(ecount[t], kEntCap);
+        const int64_t o = eoff[t];
+        for (int i = 0; i < c; ++i) {
+            const int2 e = ent[t * kEntCap + i];
+            key[o + i] = e.x;
+            val[o + i] = (int32_t)(o + i);
+            ent_t[o + i] = (int32_t)t;
+            ent_w[o + i] = __int_as_float(e.y);
+        }
+    }
+}
+
+// begin/end (pre-zeroed, [V]) of each column's range in the sorted keys.
 __global__ void dw_bounds(const int32_t *__restrict__ key, const int64_t *__restrict__ n_active,
                           int32_t *__restrict__ begin, int32_t *__restrict__ end) {
     const int64_t n = *n_active;
@@ -270,6 +321,7 @@ cudaError_t launch_dw_prep(const uint16_t *h, const int64_t *targets, const int3
                            int num_seqs, int64_t T, int64_t H, int64_t V, const float *lse,
                            const float *grad, const int64_t *order, int64_t n, const DwBuffers &b,
                            const DeviceInfo &di, cudaStream_t st) {
+    (void)di;
     const unsigned cblocks = (unsigned)((n + kScanThreads - 1) / kScanThreads);
     dw_compact_count<<<cblocks, kScanThreads, 0, st>>>(order, n, T, targets, cu, num_seqs, V,
                                                        b.scan);
@@ -279,30 +331,51 @@ cudaError_t launch_dw_prep(const uint16_t *h, const int64_t *targets, const int3
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dw_gather<<<(unsigned)n, 128, 0, st>>>(h, grad, lse, targets, b.crow, b.n_active, n, H, b.hc,
-                                           b.gc, b.lsec, b.tgtc, b.key0, b.val0);
+                                           b.gc, b.lsec, b.tgtc);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // the dZ / dZ^T GEMM appends to these lists
+    return cudaMemsetAsync(b.ecount, 0, (size_t)n * sizeof(int32_t), st);
+}
+
+cudaError_t launch_dw_entries(int64_t n, int64_t V, const DwBuffers &b, const DeviceInfo &di,
+                              cudaStream_t st) {
+    const unsigned grid_n =
+        (unsigned)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, (int64_t)di.sm_count * 8));
+    entries_count<<<grid_n, 256, 0, st>>>(b.ecount, n, b.eoff);
+    scan_counts<<<1, kScanThreads, 0, st>>>(b.eoff, n, b.etotal);
+    entries_scatter<<<grid_n, 256, 0, st>>>(b.eoff, b.ent, n, b.key0, b.val0, b.ent_t, b.ent_w,
+                                            b.ecount);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t emax = n * (int64_t)kEntCap;
     const int passes = dw_sort_passes(V);
-    const int tiles = (int)((n + kSortTile - 1) / kSortTile);
+    const int tiles = (int)((emax + kSortTile - 1) / kSortTile);
     int32_t *ks = b.key0, *vs = b.val0, *kd = b.key1, *vd = b.val1;
     for (int p = 0; p < passes; ++p) {
         const int shift = p * kRadixBits;
-        radix_histogram<<<tiles, kSortThreads, 0, st>>>(ks, b.n_active, shift, b.scan, tiles);
+        radix_histogram<<<tiles, kSortThreads, 0, st>>>(ks, b.etotal, shift, b.scan, tiles);
         scan_counts<<<1, kScanThreads, 0, st>>>(b.scan, (int64_t)tiles * kBins, nullptr);
-        radix_scatter<<<tiles, kSortThreads, 0, st>>>(ks, vs, kd, vd, b.n_active, shift, b.scan,
+        radix_scatter<<<tiles, kSortThreads, 0, st>>>(ks, vs, kd, vd, b.etotal, shift, b.scan,
                                                       tiles);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         std::swap(ks, kd);
         std::swap(vs, vd);
     }
-    const int32_t *sorted_key = ks;
     e = cudaMemsetAsync(b.begin, 0, (size_t)V * sizeof(int32_t), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(b.end, 0, (size_t)V * sizeof(int32_t), st);
     if (e != cudaSuccess) return e;
-    unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)di.sm_count * 4);
-    if (grid == 0) grid = 1;
-    dw_bounds<<<grid, 256, 0, st>>>(sorted_key, b.n_active, b.begin, b.end);
+    const unsigned grid = (unsigned)std::max<int64_t>(
+        1, std::min<int64_t>((emax + 255) / 256, (int64_t)di.sm_count * 8));
+    dw_bounds<<<grid, 256, 0, st>>>(ks, b.etotal, b.begin, b.end);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sort_entries(int32_t *ecount, int2 *ent, int64_t rows, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    const unsigned grid = (unsigned)((rows + kSortRowsPerBlock - 1) / kSortRowsPerBlock);
+    sort_entries<<<grid, 32 * kSortRowsPerBlock, 0, st>>>(ecount, ent, rows);
     return cudaGetLastError();
 }
 

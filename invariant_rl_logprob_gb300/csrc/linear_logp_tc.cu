@@ -152,8 +152,10 @@ struct TileArgs {
     // kDwK (rows = vocabulary, columns = H, K = canonical tokens)
     const uint16_t *hc;      // [n, H] canonical h
     const float *gc;         // [n] canonical g
-    const int32_t *dw_val;   // sorted canonical token indices
-    const int32_t *dw_begin, *dw_end;  // [V] range of each target
+    const int32_t *dw_idx;   // flat entry indices sorted by column
+    const int32_t *ent_t;    // flat entries: canonical token
+    const float *ent_w;      // flat entries: w = g (onehot - p) in fp32
+    const int32_t *dw_begin, *dw_end;  // [V] range of each column in dw_idx
     float *dw;               // [V, H] output
     int64_t ntok;            // kDzT: number of canonical token positions (columns)
     // tile counter (zeroed before the launch); null: static round-robin order
@@ -163,6 +165,10 @@ struct TileArgs {
     const float *grad;  // [T] (global)
     uint16_t *dz;       // [rows][ldz] bf16
     int64_t ldz;
+    // kDz / kDzT fill, kDh reads: per (local / canonical) row, the entries of
+    // the columns kept in fp32 (count, then kEntCap (column, w bits) slots)
+    int32_t *ecount;
+    int2 *ent;
     // kDh
     const uint16_t *W;  // [V][H]
     float *dh;          // [T][H] (global)
@@ -179,6 +185,25 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
                                           unsigned *err) {
     const bool ok = mbar_wait(bar, parity, abort, err);
     return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// The backward's fp32 terms.  The target column and columns with
+// p >= kEntTau (in_fp32) leave the bf16 matrix (0 there) and go to the row's
+// entry list as (column, g (onehot - p)).  A list that would overflow can only
+// come from an lse that does not belong to the inputs: the term is then
+// dropped and RK_DEVERR_LSE raised.
+__device__ __forceinline__ bool in_fp32(float p, int64_t col, int64_t tgt, int64_t V) {
+    return col < V && (col == tgt || p >= kEntTau);
+}
+
+__device__ __noinline__ void emit_entry(float g, float p, int64_t col, int64_t tgt,
+                                        int32_t *count, int2 *list, unsigned *err) {
+    const float w = __fmul_rn(g, __fsub_rn(col == tgt ? 1.f : 0.f, p));
+    const int slot = atomicAdd(count, 1);
+    if (slot < kEntCap)
+        list[slot] = make_int2((int)col, __float_as_int(w));
+    else
+        atomicOr(err, kErrLse);
 }
 
 template <int MODE>
@@ -459,7 +484,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int64_t lrow = (int64_t)mb * 2 * BM + (int64_t)rank * BM + threadIdx.x;  // local row
             const bool in_range = lrow < a.rows;
             const int64_t grow = a.row0 + lrow;                    // global row
-            const int64_t tgt = (kMB == 1 && in_range && a.targets != nullptr) ? a.targets[grow] : -1;
+            // the row's target (forward and dZ tiles only: kDzT rows are vocabulary rows)
+            const int64_t tgt = ((MODE == kFwd || MODE == kDz) && in_range && a.targets != nullptr)
+                                    ? a.targets[grow]
+                                    : -1;
             const int n0 = nb * BN;
             const uint32_t empty_bar = mapa_shared(smem_u32(&ctl->tmem_empty[b]), 0);
             if constexpr (MODE == kFwd || MODE == kGreedy) {
@@ -546,6 +574,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const float g = (kSoft && active) ? a.grad[grow] : 0.f;
                 const float nl = (kSoft && active) ? __fmul_rn(-a.lse[grow], kLog2e) : 0.f;
                 const int valid = min(BN, a.V - n0);
+                // the target's column within this tile (or out of [0, BN))
+                const int trel = (tgt >= n0 && tgt < (int64_t)n0 + BN) ? (int)(tgt - n0) : -1;
                 if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
                 tc_fence_after();
                 const uint32_t taddr = tmem + lane_off + (uint32_t)(b * BN);
@@ -556,6 +586,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
                     tmem_ld_wait();
                     uint32_t pk[16];
+                    uint32_t big = 0;  // kDz: columns of this chunk kept in fp32
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         float d0, d1;
@@ -563,13 +594,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             const float p0 = ex2(__fmaf_rn(__uint_as_float(r[2 * j]), kLog2e, nl));
                             const float p1 =
                                 ex2(__fmaf_rn(__uint_as_float(r[2 * j + 1]), kLog2e, nl));
-                            d0 = active ? __fmul_rn(g, p0) : 0.f;
-                            d1 = active ? __fmul_rn(g, p1) : 0.f;
+                            // 32-bit test of in_fp32 relative to the tile
+                            const int k0 = c * 32 + 2 * j;
+                            const bool b0 = active && k0 < valid && (k0 == trel || p0 >= kEntTau);
+                            const bool b1 =
+                                active && k0 + 1 < valid && (k0 + 1 == trel || p1 >= kEntTau);
+                            big |= (b0 ? 1u : 0u) << (2 * j);
+                            big |= (b1 ? 1u : 0u) << (2 * j + 1);
+                            d0 = (active && !b0) ? __fmul_rn(g, p0) : 0.f;
+                            d1 = (active && !b1) ? __fmul_rn(g, p1) : 0.f;
                         } else {
                             d0 = __uint_as_float(r[2 * j]);
                             d1 = __uint_as_float(r[2 * j + 1]);
                         }
                         pk[j] = pack_bf16x2(d0, d1);
+                    }
+                    if constexpr (kSoft) {
+                        if (big) {  // rare: the target's tile, or a large p
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                if ((big >> k) & 1u)
+                                    emit_entry(g, ex2(__fmaf_rn(__uint_as_float(r[k]), kLog2e, nl)),
+                                               (int64_t)n0 + c * 32 + k, tgt, a.ecount + lrow,
+                                               a.ent + lrow * kEntCap, a.err);
+                        }
                     }
                     if constexpr (kSoft) {
                         if (a.dz_tma || a.dzT_store) {
@@ -642,18 +690,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
                     const int c0 = c * 32;
                     if (c0 < tvalid) {  // the same for the whole warp
+                        // lane j holds token column c0 + j's target, -lse log2e and g
+                        const bool okl = c0 + lane < tvalid;
+                        const int tl = n0 + c0 + lane;
+                        const int tgl = okl ? (int)a.targets[tl] : -1;
+                        const float nll = okl ? __fmul_rn(-a.lse[tl], kLog2e) : 0.f;
+                        const float gl = okl ? a.grad[tl] : 0.f;
                         uint32_t pk[16];
+                        uint32_t big = 0;
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const int t0 = n0 + c0 + 2 * j;
-                            const bool ok0 = c0 + 2 * j < tvalid, ok1 = c0 + 2 * j + 1 < tvalid;
-                            const float nl0 = ok0 ? __fmul_rn(-a.lse[t0], kLog2e) : 0.f;
-                            const float nl1 = ok1 ? __fmul_rn(-a.lse[t0 + 1], kLog2e) : 0.f;
-                            const float g0 = ok0 ? a.grad[t0] : 0.f;
-                            const float g1 = ok1 ? a.grad[t0 + 1] : 0.f;
+                            const int tg0 = __shfl_sync(0xffffffffu, tgl, 2 * j);
+                            const int tg1 = __shfl_sync(0xffffffffu, tgl, 2 * j + 1);
+                            const float nl0 = __shfl_sync(0xffffffffu, nll, 2 * j);
+                            const float nl1 = __shfl_sync(0xffffffffu, nll, 2 * j + 1);
+                            const float g0 = __shfl_sync(0xffffffffu, gl, 2 * j);
+                            const float g1 = __shfl_sync(0xffffffffu, gl, 2 * j + 1);
                             const float p0 = ex2(__fmaf_rn(__uint_as_float(r[2 * j]), kLog2e, nl0));
                             const float p1 = ex2(__fmaf_rn(__uint_as_float(r[2 * j + 1]), kLog2e, nl1));
-                            pk[j] = pack_bf16x2(__fmul_rn(g0, p0), __fmul_rn(g1, p1));
+                            // token t's fp32 entries, as kDz makes them for row t
+                            const bool a0 = vrow && tg0 >= 0, a1 = vrow && tg1 >= 0;
+                            const bool b0 = a0 && in_fp32(p0, lrow, tg0, a.V);
+                            const bool b1 = a1 && in_fp32(p1, lrow, tg1, a.V);
+                            big |= (b0 ? 1u : 0u) << (2 * j);
+                            big |= (b1 ? 1u : 0u) << (2 * j + 1);
+                            pk[j] = pack_bf16x2((a0 && !b0) ? __fmul_rn(g0, p0) : 0.f,
+                                                (a1 && !b1) ? __fmul_rn(g1, p1) : 0.f);
+                        }
+                        if (__any_sync(0xffffffffu, big != 0)) {  // rare
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                const int tgk = __shfl_sync(0xffffffffu, tgl, k);
+                                const float nlk = __shfl_sync(0xffffffffu, nll, k);
+                                const float gk = __shfl_sync(0xffffffffu, gl, k);
+                                if ((big >> k) & 1u) {
+                                    const int tk = n0 + c0 + k;
+                                    emit_entry(gk, ex2(__fmaf_rn(__uint_as_float(r[k]), kLog2e, nlk)),
+                                               lrow, tgk, a.ecount + tk, a.ent + (int64_t)tk * kEntCap,
+                                               a.err);
+                                }
+                            }
                         }
                         if (a.dz_tma) {
                             // the warp's 32 x 32 block through one TMA store, as
@@ -698,8 +774,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll 1
                 for (int j = 0; j < kMB; ++j) {
-                    // vrow is a vocabulary row; its one-hot term runs over the
-                    // canonical tokens whose target it is, in canonical order
+                    // vrow is a vocabulary row; its fp32 term runs over the
+                    // entries of column vr (the tokens whose target it is or
+                    // where its p >= kEntTau), in canonical token order
                     const int64_t vr = ((int64_t)mb * kMB + j) * 2 * BM + (int64_t)rank * BM + threadIdx.x;
                     const bool vrow = vr < a.V;
                     const int32_t b0 = vrow ? a.dw_begin[vr] : 0;
@@ -717,8 +794,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int jj = 0; jj < 32; ++jj) sacc[jj] = 0.f;
                             for (int32_t i = b0; i < b1; ++i) {
-                                const int32_t tok = a.dw_val[i];
-                                const float w = a.gc[tok];
+                                const int32_t idx = a.dw_idx[i];
+                                const int32_t tok = a.ent_t[idx];
+                                const float w = a.ent_w[idx];
                                 const uint4 *src = reinterpret_cast<const uint4 *>(
                                     a.hc + (int64_t)tok * a.H + n0 + c * 32);
 #pragma unroll
@@ -757,8 +835,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int64_t gr = a.row0 + lr;
                     const int64_t tg = inr ? a.targets[gr] : -1;
                     const bool active = inr && row_active(gr, tg, a.cu, a.num_seqs) && tg < a.V;
-                    const float g = active ? a.grad[gr] : 0.f;
-                    const uint16_t *wrow = a.W + (active ? tg : 0) * (int64_t)a.H + n0;
+                    // the row's fp32 entries (target column, columns with
+                    // p >= kEntTau), sorted by column
+                    const int cnt = active ? min(a.ecount[lr], kEntCap) : 0;
+                    const int2 *el = a.ent + lr * kEntCap;
+                    const int2 e0 = cnt > 0 ? el[0] : make_int2(0, 0);  // usually the only one
                     const int hvalid = min(BN, a.H - n0);  // a multiple of 64
                     // canonical rows scatter to their physical rows; padding
                     // positions (inactive) are not stored
@@ -774,20 +855,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (store && c * 32 < hvalid) {
                             float o[32];
                             if (active) {
-                                uint4 wv[4];
-                                const uint4 *src = reinterpret_cast<const uint4 *>(wrow + c * 32);
+                                float sacc[32];
 #pragma unroll
-                                for (int qq = 0; qq < 4; ++qq) wv[qq] = __ldg(src + qq);
+                                for (int jj = 0; jj < 32; ++jj) sacc[jj] = 0.f;
+                                for (int e = 0; e < cnt; ++e) {
+                                    const int2 en = (e == 0) ? e0 : el[e];
+                                    const float w = __int_as_float(en.y);
+                                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                                        a.W + (int64_t)en.x * a.H + n0 + c * 32);
 #pragma unroll
-                                for (int qq = 0; qq < 4; ++qq) {
-                                    const uint32_t w4[4] = {wv[qq].x, wv[qq].y, wv[qq].z, wv[qq].w};
+                                    for (int qq = 0; qq < 4; ++qq) {
+                                        const uint4 v4 = __ldg(src + qq);
+                                        const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-                                    for (int u = 0; u < 4; ++u) {
-                                        const int jj = qq * 8 + u * 2;
-                                        o[jj] = __fmaf_rn(g, bf16_lo(w4[u]), -__uint_as_float(r[jj]));
-                                        o[jj + 1] = __fmaf_rn(g, bf16_hi(w4[u]), -__uint_as_float(r[jj + 1]));
+                                        for (int u = 0; u < 4; ++u) {
+                                            const int jj = qq * 8 + u * 2;
+                                            sacc[jj] = __fmaf_rn(w, bf16_lo(w4[u]), sacc[jj]);
+                                            sacc[jj + 1] = __fmaf_rn(w, bf16_hi(w4[u]), sacc[jj + 1]);
+                                        }
                                     }
                                 }
+#pragma unroll
+                                for (int jj = 0; jj < 32; ++jj) o[jj] = __fsub_rn(sacc[jj], __uint_as_float(r[jj]));
                             } else {
 #pragma unroll
                                 for (int jj = 0; jj < 32; ++jj) o[jj] = 0.f;
@@ -1135,9 +1224,13 @@ size_t linear_dw_workspace_bytes(int64_t n, int64_t H, int64_t V) {
     b += round256(ln * 8) + round256(8);                    // crow, n_active
     b += round256(ln * (size_t)H * 2);                      // hc
     b += 2 * round256(ln * 4) + round256(ln * 8);           // gc, lsec, tgtc
-    b += 4 * round256(ln * 4);                              // sort buffers
+    const size_t le = ln * (size_t)kEntCap;                 // entries, at most
+    b += round256(ln * 4) + round256(le * 8);               // ecount, ent
+    b += round256(ln * 4) + round256(8);                    // eoff, etotal
+    b += 2 * round256(le * 4);                              // ent_t, ent_w
+    b += 4 * round256(le * 4);                              // sort buffers
     b += 2 * round256((size_t)V * 4);                       // begin, end
-    b += round256((size_t)dw_scan_entries(n) * 4);          // scan counts
+    b += round256((size_t)dw_scan_entries((int64_t)le) * 4);  // scan counts
     // dZ [n][round_up(V, 8)] or dZ^T [V][round_up(n, 8)], whichever is larger
     b += round256(std::max(ln * (size_t)ld_dz(V), (size_t)V * (size_t)ld_dzt(n)) * 2);
     return b;
@@ -1207,13 +1300,20 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     bf.gc = reinterpret_cast<float *>(take(ln * 4));
     bf.lsec = reinterpret_cast<float *>(take(ln * 4));
     bf.tgtc = reinterpret_cast<int64_t *>(take(ln * 8));
-    bf.key0 = reinterpret_cast<int32_t *>(take(ln * 4));
-    bf.val0 = reinterpret_cast<int32_t *>(take(ln * 4));
-    bf.key1 = reinterpret_cast<int32_t *>(take(ln * 4));
-    bf.val1 = reinterpret_cast<int32_t *>(take(ln * 4));
+    const size_t le = ln * (size_t)kEntCap;
+    bf.ecount = reinterpret_cast<int32_t *>(take(ln * 4));
+    bf.ent = reinterpret_cast<int2 *>(take(le * 8));
+    bf.eoff = reinterpret_cast<int32_t *>(take(ln * 4));
+    bf.etotal = reinterpret_cast<int64_t *>(take(8));
+    bf.ent_t = reinterpret_cast<int32_t *>(take(le * 4));
+    bf.ent_w = reinterpret_cast<float *>(take(le * 4));
+    bf.key0 = reinterpret_cast<int32_t *>(take(le * 4));
+    bf.val0 = reinterpret_cast<int32_t *>(take(le * 4));
+    bf.key1 = reinterpret_cast<int32_t *>(take(le * 4));
+    bf.val1 = reinterpret_cast<int32_t *>(take(le * 4));
     bf.begin = reinterpret_cast<int32_t *>(take((size_t)V * 4));
     bf.end = reinterpret_cast<int32_t *>(take((size_t)V * 4));
-    bf.scan = reinterpret_cast<int32_t *>(take((size_t)dw_scan_entries(n) * 4));
+    bf.scan = reinterpret_cast<int32_t *>(take((size_t)dw_scan_entries((int64_t)le) * 4));
     bf.ldz = ld_dz(V);
     bf.dz = reinterpret_cast<uint16_t *>(
         take(std::max(ln * (size_t)bf.ldz, (size_t)V * (size_t)ld_dzt(n)) * 2));
@@ -1227,8 +1327,11 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     CUtensorMap tmHc, tmW;
     const bool sorted_in_0 = dw_sort_passes(V) % 2 == 0;
     // dW = S - dZ^T h with A = dZ^T read K-major (rows = vocabulary, columns =
-    // H, K = canonical tokens), B = h read MN-major
+    // H, K = canonical tokens), B = h read MN-major; S from the sorted flat
+    // list of fp32 entries
     auto run_dw = [&]() -> cudaError_t {
+        cudaError_t e2 = launch_dw_entries(n, V, bf, di, st);
+        if (e2 != cudaSuccess) return e2;
         CUtensorMap tmDzTk, tmHcT2;
         if (!encode_tmap_bf16_2d(&tmDzTk, dzT, (uint64_t)n, (uint64_t)V, (uint64_t)ldn * 2, BK, BM,
                                  true))
@@ -1244,8 +1347,9 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
         d.H = (int32_t)H;
         d.err = di.err;
         d.hc = bf.hc;
-        d.gc = bf.gc;
-        d.dw_val = sorted_in_0 ? bf.val0 : bf.val1;
+        d.dw_idx = sorted_in_0 ? bf.val0 : bf.val1;
+        d.ent_t = bf.ent_t;
+        d.ent_w = bf.ent_w;
         d.dw_begin = bf.begin;
         d.dw_end = bf.end;
         d.dw = dW;
@@ -1265,7 +1369,9 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
             return cudaErrorInvalidValue;
         TileArgs t{};
         t.tile_counter = counter;
-        t.targets = nullptr;
+        t.targets = bf.tgtc;  // each token column's target
+        t.ecount = bf.ecount;
+        t.ent = bf.ent;
         t.rows = V;
         t.V = (int32_t)V;
         t.H = (int32_t)H;
@@ -1308,6 +1414,8 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     a.grad = bf.gc;
     a.dz = bf.dz;
     a.ldz = bf.ldz;
+    a.ecount = bf.ecount;
+    a.ent = bf.ent;
     a.num_m = (int32_t)((n + 2 * BM - 1) / (2 * BM));
     a.num_n = (int32_t)((V + BN - 1) / BN);
     a.num_k = (int32_t)(H / BK);
@@ -1330,6 +1438,8 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     if (dh) {
         // dh over the canonical rows, K = V ascending, each row stored at its
         // physical position (the same arithmetic per row as rk_linear_logp_bwd)
+        e = launch_sort_entries(bf.ecount, bf.ent, n, st);
+        if (e != cudaSuccess) return e;
         CUtensorMap tmDz, tmWmn;
         if (!encode_tmap_bf16_2d(&tmDz, bf.dz, (uint64_t)V, (uint64_t)n, (uint64_t)bf.ldz * 2, BK,
                                  BM, true))
@@ -1351,8 +1461,12 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
 
 int64_t linear_bwd_chunk_quantum() { return BM; }
 
+// Backward workspace for a chunk of rows: tile counter, the rows' entry
+// counts and entry lists, then dZ.
 size_t linear_bwd_chunk_bytes(int64_t rows, int64_t V) {
-    return kCounterBytes + round256((size_t)rows * (size_t)ld_dz(V) * 2);
+    const size_t r = (size_t)rows;
+    return kCounterBytes + round256(r * 4) + round256(r * (size_t)kEntCap * 8) +
+           round256(r * (size_t)ld_dz(V) * 2);
 }
 
 cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
@@ -1362,13 +1476,18 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
     if (T == 0) return cudaSuccess;
     const int64_t ldz = ld_dz(V);
     // rows per chunk: as many whole 128-row blocks as the workspace holds
-    // after the tile counter
+    const size_t per_row = 4 + (size_t)kEntCap * 8 + (size_t)ldz * 2;
     if (workspace_bytes < kCounterBytes) return cudaErrorInvalidValue;
-    int64_t chunk = (int64_t)((workspace_bytes - kCounterBytes) / ((size_t)ldz * 2)) / BM * BM;
+    int64_t chunk = (int64_t)((workspace_bytes - kCounterBytes) / per_row) / BM * BM;
+    while (chunk > 0 && linear_bwd_chunk_bytes(chunk, V) > workspace_bytes) chunk -= BM;
     if (chunk <= 0) return cudaErrorInvalidValue;
     if (chunk > T) chunk = T;
-    unsigned *counter = reinterpret_cast<unsigned *>(workspace);
-    uint16_t *dz = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(workspace) + kCounterBytes);
+    uint8_t *w = reinterpret_cast<uint8_t *>(workspace);
+    unsigned *counter = reinterpret_cast<unsigned *>(w);
+    int32_t *ecount = reinterpret_cast<int32_t *>(w + kCounterBytes);
+    int2 *ent = reinterpret_cast<int2 *>(w + kCounterBytes + round256((size_t)chunk * 4));
+    uint16_t *dz = reinterpret_cast<uint16_t *>(w + kCounterBytes + round256((size_t)chunk * 4) +
+                                                round256((size_t)chunk * (size_t)kEntCap * 8));
 
     CUtensorMap tmW_k, tmW_mn;
     if (!encode_tmap_bf16_2d(&tmW_k, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2, true))
@@ -1402,9 +1521,14 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
         a.ldz = ldz;
         a.W = W;
         a.dh = dh;
+        a.ecount = ecount;
+        a.ent = ent;
         a.num_m = (int32_t)((rows + 2 * BM - 1) / (2 * BM));
 
-        // GEMM 1: z recomputed, dZ = g exp(z - lse) in bf16, stored by TMA
+        // GEMM 1: z recomputed, dZ = g exp(z - lse) in bf16 (the target and
+        // p >= 1/64 columns as fp32 entries instead), stored by TMA
+        cudaError_t e = cudaMemsetAsync(ecount, 0, (size_t)rows * 4, st);
+        if (e != cudaSuccess) return e;
         CUtensorMap tmDzS;
         if (!encode_tmap_bf16_2d_sw64(&tmDzS, dz, (uint64_t)V, (uint64_t)rows, (uint64_t)ldz * 2, 32,
                                       32))
@@ -1412,11 +1536,14 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
         a.num_n = (int32_t)((V + BN - 1) / BN);
         a.num_k = (int32_t)(H / BK);
         a.dz_tma = true;
-        cudaError_t e = run_tiles<kDz>(tmH, tmW_k, a, di, st, nullptr, &tmDzS);
+        e = run_tiles<kDz>(tmH, tmW_k, a, di, st, nullptr, &tmDzS);
         if (e != cudaSuccess) return e;
         a.dz_tma = false;
+        e = launch_sort_entries(ecount, ent, rows, st);
+        if (e != cudaSuccess) return e;
 
-        // GEMM 2: dh = g W[target] - dZ W, K = V in one ascending pass
+        // GEMM 2: dh = (the row's fp32 entries) . W - dZ W, K = V in one
+        // ascending pass
         a.num_n = (int32_t)((H + BN - 1) / BN);
         a.num_k = (int32_t)((V + BK - 1) / BK);
         e = run_rows<kDh, kDh2>(tmDz, tmW_mn, a, di, st);

@@ -19,6 +19,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Device error word bits (same values as RK_DEVERR_* in rk.h).
 constexpr unsigned kErrTargetRange = 0x1u;
 constexpr unsigned kErrTimeout = 0x2u;
+constexpr unsigned kErrLse = 0x4u;
 
 // A pipeline wait gives up after this long (global timer, ns) and the kernel
 // reports kErrTimeout instead of hanging.

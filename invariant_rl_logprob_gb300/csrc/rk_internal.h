@@ -65,6 +65,19 @@ cudaError_t launch_grpo_token(const float *logp, const float *logp_old, const fl
                               float scale, float *loss, float *grad, float *ratio, float *kl,
                               const DeviceInfo &di, cudaStream_t st);
 
+// ---- backward: columns handled exactly in fp32 ----
+// In every backward row, the target column and every column with
+// p = exp(z - lse) >= kEntTau leave the bf16 g*softmax matrix (they are
+// stored there as 0).  Their contribution w = g*(onehot - p) is kept in fp32
+// as a per-row list of (column, w) entries, at most kEntCap of them (at most
+// 1/kEntTau columns can reach kEntTau since the p of a row sum to 1, plus the
+// target).  The lists are filled in any order and then sorted by column, so
+// every later sum over them runs in one fixed order.
+constexpr int kEntCap = 65;
+constexpr float kEntTau = 1.0f / 64.0f;
+// Sorts each of the first `rows` lists by column (one warp per row).
+cudaError_t launch_sort_entries(int32_t *ecount, int2 *ent, int64_t rows, cudaStream_t st);
+
 // ---- linear_logp weight gradient (dw_prep.cu, linear_logp_tc.cu) ----
 struct DwBuffers {
     int64_t *crow;      // [n] physical row of each canonical token
@@ -73,15 +86,21 @@ struct DwBuffers {
     float *gc;          // [n] canonical upstream gradient (0 past n_active)
     float *lsec;        // [n] canonical lse
     int64_t *tgtc;      // [n] canonical targets (-1 past n_active)
-    int32_t *key0, *val0, *key1, *val1;  // [n] sort buffers
-    int32_t *begin, *end;                // [V] each target's range in the sorted list
-    int32_t *scan;      // [dw_scan_entries(n)] block counts and digit histograms
+    int32_t *ecount;    // [n] entries of each canonical token
+    int2 *ent;          // [n][kEntCap] (column, w bits) of each canonical token
+    int32_t *eoff;      // [n] offset of each token's entries in the flat list
+    int64_t *etotal;    // [1] entries in the flat list
+    int32_t *ent_t;     // [n*kEntCap] flat list: token of each entry
+    float *ent_w;       // [n*kEntCap] flat list: w of each entry
+    int32_t *key0, *val0, *key1, *val1;  // [n*kEntCap] sort buffers (column, flat index)
+    int32_t *begin, *end;                // [V] each column's range in the sorted list
+    int32_t *scan;      // [dw_scan_entries(n*kEntCap)] block counts and digit histograms
     uint16_t *dz;       // [n, ldz] bf16 canonical g * softmax
     int64_t ldz;
 };
 size_t linear_dw_workspace_bytes(int64_t n, int64_t H, int64_t V);
 int64_t dw_scan_entries(int64_t n);
-// radix passes of the target sort: the sorted list ends in (key0, val0) when
+// radix passes of the column sort: the sorted list ends in (key0, val0) when
 // even, in (key1, val1) when odd
 int dw_sort_passes(int64_t V);
 size_t linear_bwd_full_workspace_bytes(int64_t n, int64_t H, int64_t V);
@@ -89,6 +108,12 @@ cudaError_t launch_dw_prep(const uint16_t *h, const int64_t *targets, const int3
                            int num_seqs, int64_t T, int64_t H, int64_t V, const float *lse,
                            const float *grad, const int64_t *order, int64_t n, const DwBuffers &b,
                            const DeviceInfo &di, cudaStream_t st);
+// After the dZ (or dZ^T) GEMM over the canonical tokens has filled the entry
+// lists: flatten them in canonical token order, sort the flat list by column
+// (stable, so each column's entries stay in token order) and find each
+// column's [begin, end) range.
+cudaError_t launch_dw_entries(int64_t n, int64_t V, const DwBuffers &b, const DeviceInfo &di,
+                              cudaStream_t st);
 cudaError_t launch_linear_dw(const uint16_t *h, const uint16_t *W, const int64_t *targets,
                              const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
                              const float *lse, const float *grad, const int64_t *order, int64_t n,

@@ -57,7 +57,9 @@ def test_host_only_calls(lib):
     g = lib.rk_linear_logp_bwd_workspace_size
     g.restype = ctypes.c_size_t
     g.argtypes = [ctypes.c_int64] * 3
-    assert g(100, 64, 1001) == 256 + 128 * 1008 * 2
+    # tile counter, then per 128-row chunk: entry counts, entry lists
+    # (65 slots of 8 bytes), dZ; each part rounded to 256 bytes
+    assert g(100, 64, 1001) == 256 + 512 + 128 * 65 * 8 + 128 * 1008 * 2
 
 
 def test_argument_errors_return_before_any_launch(lib):

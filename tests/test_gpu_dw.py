@@ -37,7 +37,8 @@ def _gpu_dw(rk, h, W, tg, g, cu=None, order=None):
     return rk.linear_logp_dw(hd, Wd, tgd, lse, gd, cuda(cu), row_order=cuda(order))
 
 
-@pytest.mark.parametrize("T,H,V", [(64, 256, 4096), (300, 128, 1001), (129, 192, 700), (7, 64, 5)])
+@pytest.mark.parametrize("T,H,V", [(64, 256, 4096), (300, 128, 1001), (129, 192, 700), (7, 64, 5),
+                                   (200, 8192, 1500)])
 def test_dw_vs_oracle(rk, T, H, V):
     h, W, tg, g = _case(T, H, V, 5000 + T + V)
     tg[::11] = -100
@@ -136,4 +137,50 @@ def test_one_and_two_row_blocks_per_tile_agree(rk):
     dw_one = rk.linear_logp_dw(hd, Wd, tg2, lse, gd, row_order=torch.arange(10000, device=DEV))
     dw_two = rk.linear_logp_dw(hd, Wd, tg2, lse, gd)
     assert same_bits(dw_one, dw_two)
+    assert rk.get_device_error() == 0
+
+
+@pytest.mark.parametrize("w_std,argmax_targets", [(0.25, True), (0.4, True), (0.4, False)])
+def test_peaked_softmax_gradients(rk, w_std, argmax_targets):
+    # Logits with std ~6-9: most rows put p > 0.5 on one column.  With the
+    # target there (a confident, correct policy) dh = g (1 - p_t) (W_t - ...)
+    # is a small difference of large terms; with a random target two large
+    # terms compete.  The target and every column with p >= 1/64 are kept in
+    # fp32, so dh and dW stay inside the tolerance in both regimes.
+    T, H, V = 512, 512, 4096
+    gen = synth.generator(123)
+    W = synth.normal_bf16(gen, (V, H), w_std)
+    h = synth.normal_bf16(gen, (T, H), 1.0)
+    z = oracle.lm_head(bits_np(h), bits_np(W))
+    if argmax_targets:
+        tg = torch.as_tensor(z.argmax(axis=1), dtype=torch.int64)
+    else:
+        tg = synth.uniform_targets(gen, T, V)
+    g = torch.randn(T, generator=gen, dtype=torch.float32)
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    _, lse = rk.linear_logp(hd, Wd, tgd)
+    dh = rk.linear_logp_bwd(hd, Wd, tgd, lse, gd).cpu().numpy()
+    ref = oracle.linear_logp_bwd(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy())
+    chk = contract.check_gradient_accuracy(dh, ref)
+    assert chk.passed, ("dh", chk)
+    dW = rk.linear_logp_dw(hd, Wd, tgd, lse, gd).cpu().numpy()
+    refw = oracle.linear_logp_dw(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy())
+    chk = contract.check_gradient_accuracy(dW, refw)
+    assert chk.passed, ("dW", chk)
+    # and the fused full backward gives the same bits
+    dh2, dW2 = rk.linear_logp_bwd_full(hd, Wd, tgd, lse, gd)
+    assert same_bits(dh2.cpu(), torch.from_numpy(dh)) and same_bits(dW2.cpu(), torch.from_numpy(dW))
+    assert rk.get_device_error() == 0
+
+
+def test_foreign_lse_is_flagged(rk):
+    # an lse that does not belong to the inputs (here 10 too small) makes far
+    # more than 64 columns per row look like p >= 1/64: the call still
+    # finishes and raises RK_DEVERR_LSE
+    h, W, tg, g = _case(64, 256, 4096, 7)
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    _, lse = rk.linear_logp(hd, Wd, tgd)
+    rk.get_device_error()
+    rk.linear_logp_bwd(hd, Wd, tgd, lse - 10.0, gd)
+    assert rk.get_device_error() & rk.DEVERR_LSE
     assert rk.get_device_error() == 0

@@ -245,6 +245,26 @@ def test_backward_chunking_is_invisible(rk):
     assert same_bits(full, chunked)
 
 
+def test_wide_hidden_size(rk):
+    # H = 16384: 256 K stages per forward tile and 64 H tiles in the dh GEMM
+    # (four raster groups of 16)
+    gen = synth.generator(99)
+    T, H, V = 300, 16384, 3000
+    W = synth.normal_bf16(gen, (V, H), 0.01)
+    h = synth.normal_bf16(gen, (T, H), 1.0)
+    tg = synth.uniform_targets(gen, T, V)
+    g = torch.randn(T, generator=gen, dtype=torch.float32)
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    logp, lse = rk.linear_logp(hd, Wd, tgd)
+    dh = rk.linear_logp_bwd(hd, Wd, tgd, lse, gd)
+    rows = synth.sample_rows(T, 24, seed=4)
+    ref_logp, ref_lse = oracle_linear(bits_np(h), bits_np(W), tg.numpy(), rows=rows)
+    _check_fwd(logp[rows], lse[rows], ref_logp, ref_lse, "H=16384")
+    ref_dh = oracle_bwd(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy(), rows=rows)
+    _check_bwd(dh[rows], ref_dh, "H=16384")
+    assert rk.get_device_error() == 0
+
+
 def test_many_short_tiles(rk):
     # H = 64 gives one K stage per forward / dZ tile, so the producer runs
     # many tiles ahead of the epilogue and the tile queue wraps many times
