@@ -8,8 +8,13 @@
 //   logp[t] = z[t, target_t] - lse[t];   z never leaves the chip.
 // Backward with respect to h (issue #244 "[WS1 Test] ...", Workstream 3 #153:
 // fixed, batch-shape-independent reduction order, no atomicAdd):
-//   dZ[t, v] = g[t] exp(z[t, v] - lse[t])                     (GEMM 1, stored bf16)
-//   dh[t, :] = g[t] W[target_t, :] - sum_v dZ[t, v] W[v, :]    (GEMM 2, fp32)
+//   p[t, v]  = exp(z[t, v] - lse[t])
+//   dh[t, :] = sum over the row's fp32 entries e of w_e W[v_e, :]
+//              - sum_v dZ[t, v] W[v, :]                        (GEMM 2, fp32)
+// where the entries are the target column and the columns with p >= 1/64,
+// w = g (onehot - p) in fp32, and dZ = g p rounded to bf16 on every other
+// column, 0 on those (GEMM 1).  A peaked softmax thus never puts a large,
+// bf16-rounded term into the sum.
 //
 // One persistent, warp-specialised tile kernel serves the three GEMMs.  It
 // runs as CTA pairs (clusters of 2 on neighbouring SMs) sharing 256x256 output
@@ -30,14 +35,15 @@
 //   kFwd  the row's softmax partial over the tile's 256 vocabulary columns,
 //         m = max z, s = sum 2^((z - m) log2 e), and z[target] if the target
 //         is in the tile, written to workspace[row][tile];
-//   kDz   dZ = g exp(z - lse) rounded to bf16 (0 on inactive rows), and,
-//         for the fused full backward, dZ^T as well through TMA stores;
-//   kDh   dh = g W[target] - acc in fp32 (0 on inactive rows);
+//   kDz   dZ (0 on inactive rows) through TMA stores and, for the fused full
+//         backward, dZ^T as well; the row's fp32 entries appended to its list;
+//   kDh   dh = (the row's sorted entries) . W - acc in fp32 (0 on inactive rows);
 //   kLogits  z rounded to bf16 (the dense path's lm_head);
 //   kGreedy  kFwd plus the lowest column holding the tile maximum;
 //   kDzT  kDz's output transposed, from z^T = W h^T;
-//   kDwK  dW[v, :] = sum over canonical tokens with target v (in canonical
-//         order, fp32) of g h  -  (dZ^T h)[v, :].
+//   kDwK  dW[v, :] = sum over the entries of column v (in canonical token
+//         order, fp32) of w h  -  (dZ^T h)[v, :].
+// (kDh2 and kDwK2 are kDh and kDwK with two row blocks per tile.)
 // A second small kernel (linear_logp_merge) folds the forward partials of a
 // row in a fixed order into lse and logp.
 //
@@ -47,7 +53,9 @@
 // depend only on that row's inputs and on W (rows of a tensor-core tile do not
 // interact), never on the tile, CTA or M position that holds the row, on the
 // schedule, or on how the backward cuts T into chunks.  V is never split
-// across CTAs in the backward's sum (no split-K) and no atomics touch results.
+// across CTAs in the backward's sum (no split-K) and no atomics touch results
+// (an integer atomicAdd only hands out slots in an entry list, which is then
+// sorted by column).
 #include <algorithm>
 #include <cstring>
 
@@ -151,7 +159,6 @@ struct TileArgs {
     int32_t *pidx; // kGreedy: [rows][num_n] column of each tile's maximum
     // kDwK (rows = vocabulary, columns = H, K = canonical tokens)
     const uint16_t *hc;      // [n, H] canonical h
-    const float *gc;         // [n] canonical g
     const int32_t *dw_idx;   // flat entry indices sorted by column
     const int32_t *ent_t;    // flat entries: canonical token
     const float *ent_w;      // flat entries: w = g (onehot - p) in fp32
