@@ -52,9 +52,9 @@ WORKLOAD = ("grpo_fwd_bwd: linear_logp fwd+bwd T=65536 (64x1024) H=4096 V=128256
 #  --warmup 3 --no-cpu-baseline --no-rows`, one pass per launch), recorded with
 # the SHA-1 of the kernel source; reported only while the source still matches.
 TRAFFIC_RECORD = {
-    "source_sha1": "ccacaefb4532cd069c747c248f045cd03de3fba6",
-    "bytes_per_step": 193872404736,
-    "per_launch_gb": {"fwd": 18.78, "dZ": 36.68, "dh": 138.41},
+    "source_sha1": "2c4bb6ce4c1b2fd5a729d1f96668f051eb84f9e1",
+    "bytes_per_step": 168696078336,
+    "per_launch_gb": {"fwd": 18.78, "dZ": 36.74, "dh": 113.18},
 }
 # Unique bytes a step has to move: forward h + W + partials; dZ GEMM h + W +
 # dZ written; dh GEMM dZ + W read, dh written.

@@ -78,7 +78,7 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kThreads = kEpiThreads + 64;
 constexpr int kGroupN = 16;  // raster group (in N tiles) of the forward / dZ GEMMs
-constexpr int kGroupNDh = 16;  // raster group (in H tiles) of the dh GEMM
+constexpr int kGroupNDh = 8;  // raster group (in H tiles) of the dh and dW GEMMs
 
 // kFwd: forward partials; kDz: backward GEMM 1; kDh: backward GEMM 2;
 // kLogits: the dense path's lm_head (z stored as bf16); kGreedy: kFwd plus
