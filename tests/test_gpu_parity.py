@@ -161,7 +161,7 @@ def test_logits_path_full_config_all_rows(rk):
     assert rk.get_device_error() == 0
 
 
-@pytest.mark.parametrize("T,V", [(37, 1), (64, 7), (100, 1001), (33, 4096), (5, 40000)])
+@pytest.mark.parametrize("T,V", [(37, 1), (64, 7), (100, 1001), (33, 4096), (5, 40000), (16, 262144)])
 def test_logits_path_shapes(rk, T, V):
     z, tg, _ = synth.logits_batch(T=T, V=V, seed=T + V)
     logp, lse = rk.logp_from_logits(cuda(z), cuda(tg))
@@ -262,6 +262,24 @@ def test_wide_hidden_size(rk):
     _check_fwd(logp[rows], lse[rows], ref_logp, ref_lse, "H=16384")
     ref_dh = oracle_bwd(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy(), rows=rows)
     _check_bwd(dh[rows], ref_dh, "H=16384")
+    assert rk.get_device_error() == 0
+
+
+def test_largest_hidden_size(rk):
+    # H = 65536, the largest the kernels accept: 1024 K stages per forward tile
+    gen = synth.generator(100)
+    T, H, V = 40, 65536, 700
+    W = synth.normal_bf16(gen, (V, H), 0.005)
+    h = synth.normal_bf16(gen, (T, H), 1.0)
+    tg = synth.uniform_targets(gen, T, V)
+    g = torch.randn(T, generator=gen, dtype=torch.float32)
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    logp, lse = rk.linear_logp(hd, Wd, tgd)
+    dh = rk.linear_logp_bwd(hd, Wd, tgd, lse, gd)
+    ref_logp, ref_lse = oracle_linear(bits_np(h), bits_np(W), tg.numpy())
+    _check_fwd(logp, lse, ref_logp, ref_lse, "H=65536")
+    ref_dh = oracle_bwd(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy())
+    _check_bwd(dh, ref_dh, "H=65536")
     assert rk.get_device_error() == 0
 
 
