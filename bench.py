@@ -461,8 +461,10 @@ def run_gpu(args) -> None:
 
     # ---- end to end: host buffers in, results out, through the public API ----
     # Every step copies its inputs from pinned host memory and its results
-    # back.  Two device buffer sets let step i+1's inputs (copy stream) and
-    # step i-1's results (copy stream) move while step i computes.
+    # back.  Two device buffer sets let step i+1's inputs (host-to-device
+    # stream) and step i-1's results (device-to-host stream) move while step i
+    # computes.  (With one stream for both directions the loop stalled for
+    # 12-24 ms every few steps.)
     pin = lambda t: t.pin_memory()
     h_h, W_h, tg_h, g_h = pin(pool.h), pin(pool.W), pin(pool.targets), pin(pool.g)
     z_h = [(pin(z), pin(t)) for z, t in logits_host]
@@ -479,7 +481,8 @@ def run_gpu(args) -> None:
                      zt=torch.empty_like(zs[0][1]), logp=torch.empty_like(logp),
                      lse=torch.empty_like(lse), dh=torch.empty_like(dh),
                      zlogp=torch.empty_like(zlogp), zlse=torch.empty_like(zlse)))
-    copy_stream = torch.cuda.Stream(dev)
+    in_stream = torch.cuda.Stream(dev)
+    out_stream = torch.cuda.Stream(dev)
 
     def h2d_into(b, i):
         zh, zth = z_h[i % len(z_h)]
@@ -506,9 +509,9 @@ def run_gpu(args) -> None:
         in_ready = [torch.cuda.Event() for _ in range(2)]
         done = [torch.cuda.Event() for _ in range(2)]
         out_read = [torch.cuda.Event() for _ in range(2)]
-        with torch.cuda.stream(copy_stream):
+        with torch.cuda.stream(in_stream):
             h2d_into(sets[0], 0)
-            in_ready[0].record(copy_stream)
+            in_ready[0].record(in_stream)
         for i in range(n_steps):
             b, nb_ = sets[i % 2], sets[(i + 1) % 2]
             stream.wait_event(in_ready[i % 2])
@@ -516,16 +519,18 @@ def run_gpu(args) -> None:
                 stream.wait_event(out_read[i % 2])    # results of step i-2 read out
             compute(b)
             done[i % 2].record(stream)
-            with torch.cuda.stream(copy_stream):
-                if i + 1 < n_steps:
+            if i + 1 < n_steps:
+                with torch.cuda.stream(in_stream):
                     if i >= 1:
-                        copy_stream.wait_event(done[(i + 1) % 2])   # step i-1 done with nb_
+                        in_stream.wait_event(done[(i + 1) % 2])   # step i-1 done with nb_
                     h2d_into(nb_, i + 1)
-                    in_ready[(i + 1) % 2].record(copy_stream)
-                copy_stream.wait_event(done[i % 2])
+                    in_ready[(i + 1) % 2].record(in_stream)
+            with torch.cuda.stream(out_stream):
+                out_stream.wait_event(done[i % 2])
                 d2h_from(b)
-                out_read[i % 2].record(copy_stream)
-        stream.wait_stream(copy_stream)
+                out_read[i % 2].record(out_stream)
+        stream.wait_stream(in_stream)
+        stream.wait_stream(out_stream)
 
     e2e_run(2)
     torch.cuda.synchronize(dev)
@@ -606,8 +611,9 @@ def run_gpu(args) -> None:
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "how": "pinned host -> device copies of every step's inputs and device -> "
-                       "host copies of its dh/logp on a copy stream, double-buffered "
-                       "against the compute stream; timed from the first copy to the last"},
+                       "host copies of its dh/logp, each direction on its own stream, "
+                       "double-buffered against the compute stream; timed from the first "
+                       "copy to the last"},
         "gpu_launches": launches_per_step * args.steps,
         "gpu_launches_note": f"{launches_per_step} librk kernels per step x {args.steps} steps "
                              "in the timed region",
