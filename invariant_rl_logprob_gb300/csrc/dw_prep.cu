@@ -303,6 +303,87 @@ __global__ void dw_bounds(const int32_t *__restrict__ key, const int64_t *__rest
     }
 }
 
+// Rows with entries, in ascending order: a segment of the sorted keys starts
+// at i when i == 0 or key[i - 1] != key[i].  First half: segment starts per
+// block of kScanThreads keys.
+__global__ void __launch_bounds__(kScanThreads)
+    seg_count(const int32_t *__restrict__ key, const int64_t *__restrict__ n_keys,
+              int32_t *__restrict__ block_cnt) {
+    const int64_t n = *n_keys;
+    const int64_t i = (int64_t)blockIdx.x * kScanThreads + threadIdx.x;
+    const bool start = i < n && (i == 0 || key[i - 1] != key[i]);
+    const int c = __syncthreads_count(start);
+    if (threadIdx.x == 0) block_cnt[blockIdx.x] = c;
+}
+
+// Second half: rows[offset of the block + rank in the block] = the row.
+__global__ void __launch_bounds__(kScanThreads)
+    seg_write(const int32_t *__restrict__ key, const int64_t *__restrict__ n_keys,
+              const int32_t *__restrict__ block_ofs, int32_t *__restrict__ rows) {
+    __shared__ int warp_cnt[kScanThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t n = *n_keys;
+    const int64_t i = (int64_t)blockIdx.x * kScanThreads + threadIdx.x;
+    const bool start = i < n && (i == 0 || key[i - 1] != key[i]);
+    const unsigned m = __ballot_sync(0xffffffffu, start);
+    if (lane == 0) warp_cnt[warp] = __popc(m);
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += warp_cnt[w];
+    if (start) rows[block_ofs[blockIdx.x] + before + __popc(m & ((1u << lane) - 1u))] = key[i];
+}
+
+// The fp32 term of dW, S[v, :] = sum over column v's entries e, in canonical
+// token order, of w_e h_{t_e}: one block per (row with entries, 256-column
+// slice of H), 128 threads with 2 columns each.  Entries go through shared
+// memory 32 at a time so that the h loads of a batch overlap; the sum is one
+// fmaf chain per column in entry order.  Written into dW, whose GEMM epilogue
+// then subtracts the tensor-core part.  (A hot vocabulary row -- a token that
+// thousands of canonical tokens target -- is a long loop here but only for
+// its own 16 blocks; inside the GEMM epilogue it stalled whole tiles.)
+constexpr int kSThreads = 128;
+constexpr int kSCols = 2 * kSThreads;
+__global__ void __launch_bounds__(kSThreads)
+    dw_fp32_term(const int32_t *__restrict__ rows, const int64_t *__restrict__ n_rows,
+                 const int32_t *__restrict__ begin, const int32_t *__restrict__ end,
+                 const int32_t *__restrict__ idx, const int32_t *__restrict__ ent_t,
+                 const float *__restrict__ ent_w, const uint16_t *__restrict__ hc, int64_t H,
+                 float *__restrict__ dW) {
+    __shared__ int32_t s_t[32];
+    __shared__ float s_w[32];
+    const int64_t ncb = (H + kSCols - 1) / kSCols;
+    const int64_t items = *n_rows * ncb;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int32_t v = rows[it / ncb];
+        const int64_t col = (it % ncb) * kSCols + 2 * threadIdx.x;  // H % 64 == 0: col + 1 < H
+        const bool live = col < H;
+        const int32_t b0 = begin[v], b1 = end[v];
+        float s0 = 0.f, s1 = 0.f;
+        for (int32_t i0 = b0; i0 < b1; i0 += 32) {
+            const int m = min(32, b1 - i0);
+            __syncthreads();
+            if (threadIdx.x < m) {
+                const int32_t e = idx[i0 + threadIdx.x];
+                s_t[threadIdx.x] = ent_t[e];
+                s_w[threadIdx.x] = ent_w[e];
+            }
+            __syncthreads();
+            if (live) {
+#pragma unroll 8
+                for (int k = 0; k < m; ++k) {
+                    const uint32_t hv =
+                        *reinterpret_cast<const uint32_t *>(hc + (int64_t)s_t[k] * H + col);
+                    const float w = s_w[k];
+                    s0 = __fmaf_rn(w, bf16_lo(hv), s0);
+                    s1 = __fmaf_rn(w, bf16_hi(hv), s1);
+                }
+            }
+        }
+        if (live) *reinterpret_cast<float2 *>(dW + (int64_t)v * H + col) = make_float2(s0, s1);
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 int64_t dw_scan_entries(int64_t n) {
@@ -338,8 +419,8 @@ cudaError_t launch_dw_prep(const uint16_t *h, const int64_t *targets, const int3
     return cudaMemsetAsync(b.ecount, 0, (size_t)n * sizeof(int32_t), st);
 }
 
-cudaError_t launch_dw_entries(int64_t n, int64_t V, const DwBuffers &b, const DeviceInfo &di,
-                              cudaStream_t st) {
+cudaError_t launch_dw_entries(int64_t n, int64_t V, const DwBuffers &b, const uint16_t *hc,
+                              int64_t H, float *dW, const DeviceInfo &di, cudaStream_t st) {
     const unsigned grid_n =
         (unsigned)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, (int64_t)di.sm_count * 8));
     entries_count<<<grid_n, 256, 0, st>>>(b.ecount, n, b.eoff);
@@ -369,6 +450,17 @@ cudaError_t launch_dw_entries(int64_t n, int64_t V, const DwBuffers &b, const De
     const unsigned grid = (unsigned)std::max<int64_t>(
         1, std::min<int64_t>((emax + 255) / 256, (int64_t)di.sm_count * 8));
     dw_bounds<<<grid, 256, 0, st>>>(ks, b.etotal, b.begin, b.end);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the rows with entries, then their fp32 term written into dW
+    const unsigned sblocks = (unsigned)((emax + kScanThreads - 1) / kScanThreads);
+    seg_count<<<sblocks, kScanThreads, 0, st>>>(ks, b.etotal, b.scan);
+    scan_counts<<<1, kScanThreads, 0, st>>>(b.scan, sblocks, b.n_rows);
+    seg_write<<<sblocks, kScanThreads, 0, st>>>(ks, b.etotal, b.scan, b.rows);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dw_fp32_term<<<(unsigned)di.sm_count * 16, kSThreads, 0, st>>>(
+        b.rows, b.n_rows, b.begin, b.end, vs, b.ent_t, b.ent_w, hc, H, dW);
     return cudaGetLastError();
 }
 

@@ -158,12 +158,8 @@ struct TileArgs {
     float *ztgt;   // [rows]
     int32_t *pidx; // kGreedy: [rows][num_n] column of each tile's maximum
     // kDwK (rows = vocabulary, columns = H, K = canonical tokens)
-    const uint16_t *hc;      // [n, H] canonical h
-    const int32_t *dw_idx;   // flat entry indices sorted by column
-    const int32_t *ent_t;    // flat entries: canonical token
-    const float *ent_w;      // flat entries: w = g (onehot - p) in fp32
-    const int32_t *dw_begin, *dw_end;  // [V] range of each column in dw_idx
-    float *dw;               // [V, H] output
+    const int32_t *dw_begin, *dw_end;  // [V] range of each column's entries (empty: no S)
+    float *dw;               // [V, H] output, holding S on rows with entries
     int64_t ntok;            // kDzT: number of canonical token positions (columns)
     // tile counter (zeroed before the launch); null: static round-robin order
     unsigned *tile_counter;
@@ -781,9 +777,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll 1
                 for (int j = 0; j < kMB; ++j) {
-                    // vrow is a vocabulary row; its fp32 term runs over the
-                    // entries of column vr (the tokens whose target it is or
-                    // where its p >= kEntTau), in canonical token order
+                    // vrow is a vocabulary row; its fp32 term S (the entries of
+                    // column vr: the tokens whose target it is or where its
+                    // p >= kEntTau, in canonical token order) is already in dW
                     const int64_t vr = ((int64_t)mb * kMB + j) * 2 * BM + (int64_t)rank * BM + threadIdx.x;
                     const bool vrow = vr < a.V;
                     const int32_t b0 = vrow ? a.dw_begin[vr] : 0;
@@ -797,26 +793,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
                         tmem_ld_wait();
                         if (vrow && c * 32 < hvalid) {
+                            // the fp32 term S, already in dW for rows with entries
                             float sacc[32];
+                            if (b1 > b0) {
+                                const float4 *src = reinterpret_cast<const float4 *>(orow + c * 32);
 #pragma unroll
-                            for (int jj = 0; jj < 32; ++jj) sacc[jj] = 0.f;
-                            for (int32_t i = b0; i < b1; ++i) {
-                                const int32_t idx = a.dw_idx[i];
-                                const int32_t tok = a.ent_t[idx];
-                                const float w = a.ent_w[idx];
-                                const uint4 *src = reinterpret_cast<const uint4 *>(
-                                    a.hc + (int64_t)tok * a.H + n0 + c * 32);
-#pragma unroll
-                                for (int qq = 0; qq < 4; ++qq) {
-                                    const uint4 v4 = __ldg(src + qq);
-                                    const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-                                    for (int u = 0; u < 4; ++u) {
-                                        const int jj = qq * 8 + u * 2;
-                                        sacc[jj] = __fmaf_rn(w, bf16_lo(w4[u]), sacc[jj]);
-                                        sacc[jj + 1] = __fmaf_rn(w, bf16_hi(w4[u]), sacc[jj + 1]);
-                                    }
+                                for (int qq = 0; qq < 8; ++qq) {
+                                    const float4 v4 = src[qq];
+                                    sacc[4 * qq] = v4.x;
+                                    sacc[4 * qq + 1] = v4.y;
+                                    sacc[4 * qq + 2] = v4.z;
+                                    sacc[4 * qq + 3] = v4.w;
                                 }
+                            } else {
+#pragma unroll
+                                for (int jj = 0; jj < 32; ++jj) sacc[jj] = 0.f;
                             }
                             float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
 #pragma unroll
@@ -1237,6 +1228,7 @@ size_t linear_dw_workspace_bytes(int64_t n, int64_t H, int64_t V) {
     b += 2 * round256(le * 4);                              // ent_t, ent_w
     b += 4 * round256(le * 4);                              // sort buffers
     b += 2 * round256((size_t)V * 4);                       // begin, end
+    b += round256((size_t)V * 4) + round256(8);             // rows, n_rows
     b += round256((size_t)dw_scan_entries((int64_t)le) * 4);  // scan counts
     // dZ [n][round_up(V, 8)] or dZ^T [V][round_up(n, 8)], whichever is larger
     b += round256(std::max(ln * (size_t)ld_dz(V), (size_t)V * (size_t)ld_dzt(n)) * 2);
@@ -1320,6 +1312,8 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     bf.val1 = reinterpret_cast<int32_t *>(take(le * 4));
     bf.begin = reinterpret_cast<int32_t *>(take((size_t)V * 4));
     bf.end = reinterpret_cast<int32_t *>(take((size_t)V * 4));
+    bf.rows = reinterpret_cast<int32_t *>(take((size_t)V * 4));
+    bf.n_rows = reinterpret_cast<int64_t *>(take(8));
     bf.scan = reinterpret_cast<int32_t *>(take((size_t)dw_scan_entries((int64_t)le) * 4));
     bf.ldz = ld_dz(V);
     bf.dz = reinterpret_cast<uint16_t *>(
@@ -1332,12 +1326,11 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     if (e != cudaSuccess) return e;
 
     CUtensorMap tmHc, tmW;
-    const bool sorted_in_0 = dw_sort_passes(V) % 2 == 0;
     // dW = S - dZ^T h with A = dZ^T read K-major (rows = vocabulary, columns =
     // H, K = canonical tokens), B = h read MN-major; S from the sorted flat
     // list of fp32 entries
     auto run_dw = [&]() -> cudaError_t {
-        cudaError_t e2 = launch_dw_entries(n, V, bf, di, st);
+        cudaError_t e2 = launch_dw_entries(n, V, bf, bf.hc, H, dW, di, st);
         if (e2 != cudaSuccess) return e2;
         CUtensorMap tmDzTk, tmHcT2;
         if (!encode_tmap_bf16_2d(&tmDzTk, dzT, (uint64_t)n, (uint64_t)V, (uint64_t)ldn * 2, BK, BM,
@@ -1353,10 +1346,6 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
         d.V = (int32_t)V;
         d.H = (int32_t)H;
         d.err = di.err;
-        d.hc = bf.hc;
-        d.dw_idx = sorted_in_0 ? bf.val0 : bf.val1;
-        d.ent_t = bf.ent_t;
-        d.ent_w = bf.ent_w;
         d.dw_begin = bf.begin;
         d.dw_end = bf.end;
         d.dw = dW;

@@ -94,6 +94,8 @@ struct DwBuffers {
     float *ent_w;       // [n*kEntCap] flat list: w of each entry
     int32_t *key0, *val0, *key1, *val1;  // [n*kEntCap] sort buffers (column, flat index)
     int32_t *begin, *end;                // [V] each column's range in the sorted list
+    int32_t *rows;      // [V] the columns (rows of dW) with entries, ascending
+    int64_t *n_rows;    // [1] how many
     int32_t *scan;      // [dw_scan_entries(n*kEntCap)] block counts and digit histograms
     uint16_t *dz;       // [n, ldz] bf16 canonical g * softmax
     int64_t ldz;
@@ -112,8 +114,10 @@ cudaError_t launch_dw_prep(const uint16_t *h, const int64_t *targets, const int3
 // lists: flatten them in canonical token order, sort the flat list by column
 // (stable, so each column's entries stay in token order) and find each
 // column's [begin, end) range.
-cudaError_t launch_dw_entries(int64_t n, int64_t V, const DwBuffers &b, const DeviceInfo &di,
-                              cudaStream_t st);
+// Also writes each row's fp32 term S (the sum of its entries' w * h, in
+// canonical token order) into dW, for the dW GEMM epilogue to complete.
+cudaError_t launch_dw_entries(int64_t n, int64_t V, const DwBuffers &b, const uint16_t *hc,
+                              int64_t H, float *dW, const DeviceInfo &di, cudaStream_t st);
 cudaError_t launch_linear_dw(const uint16_t *h, const uint16_t *W, const int64_t *targets,
                              const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
                              const float *lse, const float *grad, const int64_t *order, int64_t n,

@@ -184,3 +184,26 @@ def test_foreign_lse_is_flagged(rk):
     rk.linear_logp_bwd(hd, Wd, tgd, lse - 10.0, gd)
     assert rk.get_device_error() & rk.DEVERR_LSE
     assert rk.get_device_error() == 0
+
+
+def test_skewed_targets(rk):
+    # Half the tokens share one target and a few others repeat hundreds of
+    # times (as common tokens do in real batches): long per-row entry lists
+    # for the fp32 term, which runs in batches of 32 entries.
+    T, H, V = 3000, 256, 2048
+    h, W, _, g = _case(T, H, V, 61)
+    gen = synth.generator(62)
+    tg = torch.randint(0, V, (T,), generator=gen)
+    tg[: T // 2] = 7
+    tg[T // 2: T // 2 + 400] = 1999
+    tg[T // 2 + 400: T // 2 + 433] = 0
+    tg = tg[torch.randperm(T, generator=gen)]
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    _, lse = rk.linear_logp(hd, Wd, tgd)
+    dW = rk.linear_logp_dw(hd, Wd, tgd, lse, gd)
+    ref = oracle.linear_logp_dw(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy())
+    chk = contract.check_gradient_accuracy(dW.cpu().numpy(), ref)
+    assert chk.passed, chk
+    dh2, dW2 = rk.linear_logp_bwd_full(hd, Wd, tgd, lse, gd)
+    assert same_bits(dW2, dW)
+    assert rk.get_device_error() == 0
