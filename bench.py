@@ -52,9 +52,9 @@ WORKLOAD = ("grpo_fwd_bwd: linear_logp fwd+bwd T=65536 (64x1024) H=4096 V=128256
 #  --warmup 3 --no-cpu-baseline --no-rows`, one pass per launch), recorded with
 # the SHA-1 of the kernel source; reported only while the source still matches.
 TRAFFIC_RECORD = {
-    "source_sha1": "2c4bb6ce4c1b2fd5a729d1f96668f051eb84f9e1",
-    "bytes_per_step": 168696078336,
-    "per_launch_gb": {"fwd": 18.78, "dZ": 36.74, "dh": 113.18},
+    "source_sha1": "c453b324ac3b185f18a5b1ecc5908c679976a698",
+    "bytes_per_step": 193677164544,
+    "per_launch_gb": {"fwd": 18.78, "dZ": 36.65, "dh": 138.25},
 }
 # Unique bytes a step has to move: forward h + W + partials; dZ GEMM h + W +
 # dZ written; dh GEMM dZ + W read, dh written.
@@ -339,6 +339,22 @@ def measure_rows(rk, pool, zs, peaks, dev, stream) -> dict:
                              "peak": peaks["bf16_tflops_sustained"],
                              "frac": tf / peaks["bf16_tflops_sustained"],
                              "algorithmic": "4*T*H*V flop (dZ recompute + dZ^T h)"}
+    # the same with Zipf(1.1)-distributed targets (seeded), as common tokens
+    # repeat in real batches: long entry lists on a few vocabulary rows
+    import numpy as np
+    rng = np.random.default_rng(11)
+    pz = np.arange(1, V + 1, dtype=np.float64) ** -1.1
+    tz = torch.as_tensor(rng.choice(V, size=T, p=pz / pz.sum()), dtype=torch.int64).to(dev)
+    _, lsez = rk.linear_logp(h, W, tz, stream=stream)
+    ms = time_loop(lambda i: rk.linear_logp_dw(h, W, tz, lsez, g, dW=dW, workspace=wsd,
+                                               stream=stream), 3, stream)
+    tf = 4.0 * T * H * V / (ms / 1e3) / 1e12
+    out["linear_logp_dw_zipf_targets"] = {
+        "shape": [T, H, V], "ms_per_call": ms, "bound": "tensor", "achieved": tf,
+        "unit": "TFLOP/s", "peak": peaks["bf16_tflops_sustained"],
+        "frac": tf / peaks["bf16_tflops_sustained"],
+        "top_target_count": int(torch.bincount(tz).max().item())}
+    del tz, lsez
     # the whole backward (dh + dW) from one shared softmax pass, 6*T*H*V flop
     del wsd
     wsd = torch.empty(rk.linear_logp_bwd_full_workspace_size(T, H, V), dtype=torch.uint8,
