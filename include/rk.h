@@ -246,7 +246,8 @@ rk_status rk_linear_greedy(const uint16_t *h, const uint16_t *W, const int32_t *
  * p >= 1/64 are handled in fp32: per vocabulary row, the fp32 terms
  * g (onehot - p) h_i are summed over those tokens in canonical order.  The
  * remaining g p h_i terms are a tensor-core GEMM with K = the canonical
- * tokens in one ascending pass.
+ * tokens in one ascending pass.  An lse that does not belong to the inputs
+ * sets RK_DEVERR_LSE as in rk_linear_logp_bwd.
  */
 size_t rk_linear_logp_dw_workspace_size(int64_t n, int64_t H, int64_t V);
 rk_status rk_linear_logp_dw(const uint16_t *h, const uint16_t *W, const int64_t *targets,
