@@ -284,7 +284,9 @@ def measure_rows(rk, pool, zs, peaks, dev, stream) -> dict:
     # dense path lm_head on a 8192-row slice of the group (bf16 logits 2.1 GB)
     Td = 8192
     logits = torch.empty((Td, V), dtype=torch.bfloat16, device=dev)
-    ms = time_loop(lambda i: rk.lm_head(h[:Td], W, out=logits, stream=stream), 5, stream)
+    wsl = torch.empty(rk.lm_head_workspace_size(), dtype=torch.uint8, device=dev)
+    ms = time_loop(lambda i: rk.lm_head(h[:Td], W, out=logits, workspace=wsl, stream=stream), 5,
+                   stream)
     tf = 2.0 * Td * H * V / (ms / 1e3) / 1e12
     out["lm_head"] = {"shape": [Td, H, V], "ms_per_call": ms, "bound": "tensor", "achieved": tf,
                       "unit": "TFLOP/s", "peak": peaks["bf16_tflops"],

@@ -167,10 +167,18 @@ rk_status rk_linear_logp_bwd(const uint16_t *h, const uint16_t *W, const int64_t
  * for every T, so a row's logits do not depend on the batch).
  *   h bf16 [T, H], W bf16 [V, H] (16-byte aligned), logits bf16 [T, ld_logits]
  *   (16-byte aligned, ld_logits >= V and a multiple of 8; columns >= V untouched).
+ *   workspace  NULL, or >= rk_lm_head_workspace_size() bytes (16-byte aligned):
+ *              with it, the tile kernel's CTA pairs take their tiles from a
+ *              counter there, in the order they become free, which keeps the
+ *              pairs in step and L2 reuse high; without it each pair works
+ *              through a fixed list of tiles.  The logits are the same bits
+ *              either way.  Contents on entry are ignored.
  * Supported: as rk_linear_logp.  Every row is computed (no mask).
  */
+size_t rk_lm_head_workspace_size(void);
 rk_status rk_lm_head(const uint16_t *h, const uint16_t *W, int64_t T, int64_t H, int64_t V,
-                     uint16_t *logits, int64_t ld_logits, void *stream);
+                     uint16_t *logits, int64_t ld_logits, void *workspace,
+                     size_t workspace_bytes, void *stream);
 
 /*
  * Logits-path backward (the gradient of the dense path, issue #244 Workstream

@@ -29,7 +29,7 @@ __all__ = [
     "linear_logp_bwd", "linear_logp_bwd_workspace_size", "linear_logp_bwd_min_workspace_size",
     "lm_head", "logp_from_logits_bwd", "grpo_token_loss", "linear_greedy",
     "linear_greedy_workspace_size", "linear_logp_dw", "linear_logp_dw_workspace_size",
-    "linear_logp_bwd_full", "linear_logp_bwd_full_workspace_size",
+    "linear_logp_bwd_full", "linear_logp_bwd_full_workspace_size", "lm_head_workspace_size",
     "get_device_error", "selftest_wait_timeout", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT", "DEVERR_LSE",
 ]
 
@@ -81,7 +81,9 @@ def load_library() -> ctypes.CDLL:
     lib.rk_linear_logp_bwd_min_workspace_size.restype = sz
     lib.rk_linear_logp_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, sz, vp]
     lib.rk_linear_logp_bwd.restype = ctypes.c_int
-    lib.rk_lm_head.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp]
+    lib.rk_lm_head.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, sz, vp]
+    lib.rk_lm_head_workspace_size.argtypes = []
+    lib.rk_lm_head_workspace_size.restype = sz
     lib.rk_lm_head.restype = ctypes.c_int
     lib.rk_logp_from_logits_bwd.argtypes = [vp, vp, vp, i32, i64, i64, vp, vp, vp, vp]
     lib.rk_logp_from_logits_bwd.restype = ctypes.c_int
@@ -241,9 +243,17 @@ def linear_logp_bwd(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, lse
     return dh
 
 
+def lm_head_workspace_size() -> int:
+    return int(load_library().rk_lm_head_workspace_size())
+
+
 def lm_head(h: torch.Tensor, W: torch.Tensor, *, out: torch.Tensor | None = None,
+            workspace: torch.Tensor | None = None,
             stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-    """Dense path: bf16 logits ``[T, V]`` = bf16(h W^T) (fp32 accumulation)."""
+    """Dense path: bf16 logits ``[T, V]`` = bf16(h W^T) (fp32 accumulation).
+
+    ``workspace`` (uint8, >= ``rk_lm_head_workspace_size()`` bytes) holds the
+    tile counter; one is allocated when it is None."""
     lib = load_library()
     _need(h, "h", torch.bfloat16, 2)
     _need(W, "W", torch.bfloat16, 2)
@@ -259,7 +269,11 @@ def lm_head(h: torch.Tensor, W: torch.Tensor, *, out: torch.Tensor | None = None
         if out.dtype != torch.bfloat16 or out.dim() != 2 or out.stride(1) != 1:
             raise ValueError("out must be a bf16 [T, V] view with unit column stride")
         ld = out.stride(0)
-    st = lib.rk_lm_head(_ptr(h), _ptr(W), T, H, V, _ptr(out), ld, _stream_handle(stream, h.device))
+    if workspace is None:
+        workspace = torch.empty(int(lib.rk_lm_head_workspace_size()), dtype=torch.uint8,
+                                device=h.device)
+    st = lib.rk_lm_head(_ptr(h), _ptr(W), T, H, V, _ptr(out), ld, _ptr(workspace),
+                        workspace.numel(), _stream_handle(stream, h.device))
     _check(st, "rk_lm_head")
     return out
 

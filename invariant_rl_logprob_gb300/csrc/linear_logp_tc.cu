@@ -1193,7 +1193,8 @@ cudaError_t launch_linear_greedy(const uint16_t *h, const uint16_t *W, const int
 }
 
 cudaError_t launch_lm_head(const uint16_t *h, const uint16_t *W, int64_t T, int64_t H, int64_t V,
-                           uint16_t *logits, int64_t ld, const DeviceInfo &di, cudaStream_t st) {
+                           uint16_t *logits, int64_t ld, unsigned *tile_counter,
+                           const DeviceInfo &di, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     CUtensorMap tmA, tmB;
     if (!encode_tmap_bf16_2d(&tmA, h, (uint64_t)H, (uint64_t)T, (uint64_t)H * 2, BK, BM, true))
@@ -1212,6 +1213,7 @@ cudaError_t launch_lm_head(const uint16_t *h, const uint16_t *W, int64_t T, int6
     a.err = di.err;
     a.dz = logits;
     a.ldz = ld;
+    a.tile_counter = tile_counter;  // null: fixed tile lists
     return run_tiles<kLogits>(tmA, tmB, a, di, st);
 }
 

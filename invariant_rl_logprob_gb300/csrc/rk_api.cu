@@ -235,8 +235,11 @@ rk_status rk_linear_logp_bwd(const uint16_t *h, const uint16_t *W, const int64_t
     return RK_OK;
 }
 
+size_t rk_lm_head_workspace_size(void) { return 256; }
+
 rk_status rk_lm_head(const uint16_t *h, const uint16_t *W, int64_t T, int64_t H, int64_t V,
-                     uint16_t *logits, int64_t ld_logits, void *stream) {
+                     uint16_t *logits, int64_t ld_logits, void *workspace,
+                     size_t workspace_bytes, void *stream) {
     if (T < 0 || H <= 0 || V <= 0) return RK_ERR_INVALID_ARG;
     if (T == 0) return RK_OK;
     if (!h || !W || !logits || ld_logits < V) return RK_ERR_INVALID_ARG;
@@ -244,10 +247,13 @@ rk_status rk_lm_head(const uint16_t *h, const uint16_t *W, int64_t T, int64_t H,
         return RK_ERR_UNSUPPORTED;
     if (!aligned(h, 16) || !aligned(W, 16) || !aligned(logits, 16) || ld_logits % 8 != 0)
         return RK_ERR_UNSUPPORTED;
+    if (workspace && (workspace_bytes < rk_lm_head_workspace_size() || !aligned(workspace, 16)))
+        return RK_ERR_WORKSPACE;
     DeviceInfo di;
     cudaError_t e = rk::current_device_info(&di);
     if (e != cudaSuccess) return rk::cuda_fail(e);
-    e = rk::launch_lm_head(h, W, T, H, V, logits, ld_logits, di, static_cast<cudaStream_t>(stream));
+    e = rk::launch_lm_head(h, W, T, H, V, logits, ld_logits, static_cast<unsigned *>(workspace), di,
+                           static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return rk::cuda_fail(e);
     return RK_OK;
 }

@@ -50,7 +50,8 @@ cudaError_t launch_linear_greedy(const uint16_t *h, const uint16_t *W, const int
                                  float *logp, float *lse, void *workspace, const DeviceInfo &di,
                                  cudaStream_t st);
 cudaError_t launch_lm_head(const uint16_t *h, const uint16_t *W, int64_t T, int64_t H, int64_t V,
-                           uint16_t *logits, int64_t ld, const DeviceInfo &di, cudaStream_t st);
+                           uint16_t *logits, int64_t ld, unsigned *tile_counter,
+                           const DeviceInfo &di, cudaStream_t st);
 
 // ---- logits-path backward (logits_logp.cu) ----
 cudaError_t launch_logits_bwd(const uint16_t *logits, const int64_t *targets, const int32_t *cu,

@@ -82,12 +82,16 @@ def test_argument_errors_of_the_widened_rows(lib):
     vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
     lh = lib.rk_lm_head
     lh.restype = ctypes.c_int
-    lh.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp]
-    assert lh(None, None, -1, 64, 10, None, 16, None) == 1          # T < 0
-    assert lh(None, None, 0, 64, 10, None, 16, None) == 0           # T = 0: nothing to do
-    fake = ctypes.c_void_p(4096)                                     # never dereferenced
-    assert lh(fake, fake, 4, 64, 10, fake, 8, None) == 1            # ld < V
-    assert lh(fake, fake, 4, 96, 10, fake, 16, None) == 2           # H % 64 != 0
+    lh.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, sz, vp]
+    assert lh(None, None, -1, 64, 10, None, 16, None, 0, None) == 1   # T < 0
+    assert lh(None, None, 0, 64, 10, None, 16, None, 0, None) == 0    # T = 0: nothing to do
+    fake = ctypes.c_void_p(4096)                                       # never dereferenced
+    assert lh(fake, fake, 4, 64, 10, fake, 8, None, 0, None) == 1     # ld < V
+    assert lh(fake, fake, 4, 96, 10, fake, 16, None, 0, None) == 2    # H % 64 != 0
+    assert lh(fake, fake, 4, 64, 10, fake, 16, fake, 8, None) == 3    # workspace too small
+    lws = lib.rk_lm_head_workspace_size
+    lws.restype = sz
+    assert lws() == 256
     gl = lib.rk_grpo_token_loss
     gl.restype = ctypes.c_int
     gl.argtypes = [vp] * 6 + [i32, i64, f32, f32, f32, f32] + [vp] * 5

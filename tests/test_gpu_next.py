@@ -40,6 +40,22 @@ def test_lm_head_vs_oracle(rk, T, H, V):
     assert rk.get_device_error() == 0
 
 
+def test_lm_head_tile_order(rk):
+    # tiles taken from the workspace counter or from fixed per-pair lists:
+    # the same bits
+    gen = synth.generator(3100)
+    W = synth.normal_bf16(gen, (9000, 256), 0.02)
+    h = synth.normal_bf16(gen, (1500, 256), 1.0)
+    hd, Wd = cuda(h), cuda(W)
+    a = rk.lm_head(hd, Wd)
+    lib = rk.load_library()
+    b = torch.empty_like(a)
+    st = lib.rk_lm_head(hd.data_ptr(), Wd.data_ptr(), 1500, 256, 9000, b.data_ptr(), b.stride(0),
+                        None, 0, torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    assert torch.equal(a.view(torch.int16).cpu(), b.view(torch.int16).cpu())
+
+
 def test_dense_vs_indexed_paths(rk):
     # P-relation: logp from bf16 logits (dense) vs logp fused on fp32 z
     # (indexed).  The dense path rounds every z to bf16 (|dz| <= 2^-9 |z|), so
