@@ -52,9 +52,9 @@ WORKLOAD = ("grpo_fwd_bwd: linear_logp fwd+bwd T=65536 (64x1024) H=4096 V=128256
 #  --warmup 3 --no-cpu-baseline --no-rows`, one pass per launch), recorded with
 # the SHA-1 of the kernel source; reported only while the source still matches.
 TRAFFIC_RECORD = {
-    "source_sha1": "c453b324ac3b185f18a5b1ecc5908c679976a698",
-    "bytes_per_step": 193677164544,
-    "per_launch_gb": {"fwd": 18.78, "dZ": 36.65, "dh": 138.25},
+    "source_sha1": "8663de08b4ef2455b2772da1707943854d8bedb6",
+    "bytes_per_step": 160388734976,
+    "per_launch_gb": {"fwd": 18.79, "dZ": 36.77, "dh": 104.83},
 }
 # Unique bytes a step has to move: forward h + W + partials; dZ GEMM h + W +
 # dZ written; dh GEMM dZ + W read, dh written.
