@@ -44,8 +44,15 @@
  *  - Argument errors return a status before anything is launched.  Launch
  *    failures return RK_ERR_CUDA (the CUDA error is left for
  *    cudaGetLastError / rk_last_cuda_error).
- *  - Thread safety: entry points may be called from several host threads; the
- *    only shared state is a per-device cache of function pointers.
+ *  - Thread safety: entry points may be called from several host threads.
+ *    Shared state: the driver's tensor-map encoder, looked up once; per
+ *    device, the SM count and the device addresses of the library's static
+ *    device variables (the error word, rk_linear_logp_noalloc's array), looked
+ *    up on the first call on that device; the rk_set_row_blocks setting.
+ *  - Contexts: those cached addresses belong to the device's primary context
+ *    (the one the CUDA runtime uses).  After cudaDeviceReset, or with another
+ *    context current, they no longer point at this library's variables:
+ *    reload the library (a new process) before calling it again.
  */
 #ifndef RK_H
 #define RK_H
@@ -305,8 +312,8 @@ rk_status rk_linear_logp_bwd_full(const uint16_t *h, const uint16_t *W, const in
  *    about T * ceil(V/256) * 8 + T * 4 bytes; e.g. at most 8363 rows for
  *    V = 128256 and 33420 rows for V = 32000.
  *  - The first call on each device looks up that device's array address
- *    (with that device current); make that first call before any stream
- *    capture.
+ *    (with that device current) and keeps it for the life of the process (see
+ *    "Contexts" above); make that first call before any stream capture.
  *  - All calls on a device share the one array and nothing in it needs to
  *    start at zero; calls that overlap on the GPU (several streams, or
  *    several host threads at once) race on it and must be serialised.
@@ -327,11 +334,32 @@ rk_status rk_get_device_error(void *stream, int32_t *err);
  * Self-test of the failure path that every pipeline wait in the library
  * shares: one kernel waits on an mbarrier that is never completed, gives up
  * after `limit_ns` (1 ns .. 10 s) and sets RK_DEVERR_TIMEOUT in the device
- * error word, leaving the context usable.  (The pages' issue #244, #150
- * "Silent fallback ... = fail": a stalled pipeline must surface as an error,
- * never as a hang.)  Asynchronous; read the result with rk_get_device_error.
+ * error word, leaving the context usable.  (Issue #244, Workstream 4 #150
+ * chain gate: a path that quietly falls back counts as a failure, so a
+ * stalled pipeline has to come back as an error rather than a hang.)
+ * Asynchronous; read the result with rk_get_device_error.
  */
 rk_status rk_selftest_wait_timeout(int64_t limit_ns, void *stream);
+
+/*
+ * Diagnostics of the two backward GEMMs that sum over a long K axis: dh
+ * (K = vocabulary; rk_linear_logp_bwd, rk_linear_logp_bwd_full) and dW
+ * (K = canonical tokens; rk_linear_logp_dw, rk_linear_logp_bwd_full).  Each
+ * runs with one or two 256-row blocks per 256-column tile.  Two blocks share
+ * every B slice between both TMEM accumulators (half the B traffic) and are
+ * picked automatically for long K loops (>= 256 stages of 64) with enough
+ * tiles (about 8 per resident CTA pair).  Every accumulator sees the same MMA
+ * sequence in either form, so the choice never changes a bit of dh or dW.
+ *
+ * rk_set_row_blocks(n): n = 0 automatic (the default), 1 or 2 forces that
+ * form for every later launch in the process (so that tests can run either
+ * form on shapes of their choice).  RK_ERR_INVALID_ARG for other n.
+ * rk_last_row_blocks(gemm): blocks per tile of the last such GEMM launched
+ * on the calling host thread: gemm 0 = dh, 1 = dW.  Returns 1 or 2, 0 before
+ * the first launch, -1 for another gemm value.
+ */
+rk_status rk_set_row_blocks(int32_t n);
+int32_t rk_last_row_blocks(int32_t gemm);
 
 /* Human-readable name of a status code (static string). */
 const char *rk_status_string(rk_status s);

@@ -30,7 +30,7 @@ __all__ = [
     "lm_head", "logp_from_logits_bwd", "grpo_token_loss", "linear_greedy",
     "linear_greedy_workspace_size", "linear_logp_dw", "linear_logp_dw_workspace_size",
     "linear_logp_bwd_full", "linear_logp_bwd_full_workspace_size", "lm_head_workspace_size",
-    "get_device_error", "selftest_wait_timeout", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT", "DEVERR_LSE",
+    "get_device_error", "selftest_wait_timeout", "set_row_blocks", "last_row_blocks", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT", "DEVERR_LSE",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -115,6 +115,10 @@ def load_library() -> ctypes.CDLL:
     lib.rk_last_cuda_error.restype = ctypes.c_int
     lib.rk_version.argtypes = []
     lib.rk_version.restype = ctypes.c_char_p
+    lib.rk_set_row_blocks.argtypes = [i32]
+    lib.rk_set_row_blocks.restype = ctypes.c_int
+    lib.rk_last_row_blocks.argtypes = [i32]
+    lib.rk_last_row_blocks.restype = i32
     _lib = lib
     return lib
 
@@ -436,6 +440,18 @@ def selftest_wait_timeout(limit_ns: int, stream: torch.cuda.Stream | None = None
     lib = load_library()
     _check(lib.rk_selftest_wait_timeout(int(limit_ns), _stream_handle(stream, None)),
            "rk_selftest_wait_timeout")
+
+
+def set_row_blocks(n: int) -> None:
+    """Row blocks per tile of the dh and dW GEMMs: 0 automatic (default), or
+    1 / 2 forced for every later launch in the process (bits are unchanged)."""
+    _check(load_library().rk_set_row_blocks(int(n)), "rk_set_row_blocks")
+
+
+def last_row_blocks(gemm: str) -> int:
+    """Row blocks per tile of the last ``"dh"`` or ``"dw"`` GEMM launched on
+    this thread (0 before the first)."""
+    return int(load_library().rk_last_row_blocks({"dh": 0, "dw": 1}[gemm]))
 
 
 def get_device_error(stream: torch.cuda.Stream | None = None) -> int:

@@ -57,6 +57,7 @@
 // (an integer atomicAdd only hands out slots in an entry list, which is then
 // sorted by column).
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "rk_device.cuh"
@@ -1088,11 +1089,20 @@ cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tile
 // such tiles for about 8 rounds of the resident pairs; one row block per tile
 // otherwise.  Either way every accumulator sees the same MMA sequence, so the
 // choice does not change any bit.
+// A process-wide override (rk_set_row_blocks) can force either form; the
+// form each GEMM last used on this host thread is kept for rk_last_row_blocks.
+std::atomic<int> g_row_blocks_override{0};
+thread_local int g_last_row_blocks[2] = {0, 0};
+
 template <int M1, int M2>
 cudaError_t run_rows(const CUtensorMap &tmA, const CUtensorMap &tmB, const TileArgs &a,
-                     const DeviceInfo &di, cudaStream_t st) {
+                     const DeviceInfo &di, cudaStream_t st, RowGemm which) {
     const int64_t two = (int64_t)((a.num_m + 1) / 2) * a.num_n;
-    if (a.num_k >= 256 && two >= 8 * resident_pairs<M2>(di)) return run_tiles<M2>(tmA, tmB, a, di, st);
+    const int force = g_row_blocks_override.load(std::memory_order_relaxed);
+    const bool use_two =
+        force == 2 || (force == 0 && a.num_k >= 256 && two >= 8 * resident_pairs<M2>(di));
+    g_last_row_blocks[(int)which] = use_two ? 2 : 1;
+    if (use_two) return run_tiles<M2>(tmA, tmB, a, di, st);
     return run_tiles<M1>(tmA, tmB, a, di, st);
 }
 
@@ -1100,6 +1110,9 @@ int64_t ld_dz(int64_t V) { return (V + 7) / 8 * 8; }  // 16-byte aligned dZ rows
 int64_t ld_dzt(int64_t n) { return ld_dz(n); }         // dZ^T rows (tokens)
 
 }  // namespace
+
+void set_row_blocks_override(int n) { g_row_blocks_override.store(n, std::memory_order_relaxed); }
+int last_row_blocks(RowGemm which) { return g_last_row_blocks[(int)which]; }
 
 // Every launcher with a workspace keeps the tile counter of its tile
 // launches in one 256-byte slot of it.
@@ -1354,7 +1367,7 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
         d.num_m = (int32_t)((V + 2 * BM - 1) / (2 * BM));
         d.num_n = (int32_t)((H + BN - 1) / BN);
         d.num_k = (int32_t)((n + BK - 1) / BK);
-        return run_rows<kDwK, kDwK2>(tmDzTk, tmHcT2, d, di, st);
+        return run_rows<kDwK, kDwK2>(tmDzTk, tmHcT2, d, di, st, RowGemm::kDwGemm);
     };
     if (!dh) {
         // dW alone: dZ^T over the canonical tokens (z^T = W h^T, both operands
@@ -1450,7 +1463,7 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
         q.out_rows = bf.crow;
         q.num_n = (int32_t)((H + BN - 1) / BN);
         q.num_k = (int32_t)((V + BK - 1) / BK);
-        e = run_rows<kDh, kDh2>(tmDz, tmWmn, q, di, st);
+        e = run_rows<kDh, kDh2>(tmDz, tmWmn, q, di, st, RowGemm::kDhGemm);
         if (e != cudaSuccess) return e;
     }
     if (!dW) return cudaSuccess;
@@ -1544,7 +1557,7 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
         // ascending pass
         a.num_n = (int32_t)((H + BN - 1) / BN);
         a.num_k = (int32_t)((V + BK - 1) / BK);
-        e = run_rows<kDh, kDh2>(tmDz, tmW_mn, a, di, st);
+        e = run_rows<kDh, kDh2>(tmDz, tmW_mn, a, di, st, RowGemm::kDhGemm);
         if (e != cudaSuccess) return e;
     }
     linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(targets, cu, num_seqs, T, (int32_t)V,

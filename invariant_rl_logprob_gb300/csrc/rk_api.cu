@@ -122,13 +122,8 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned *err) {
     }
 }
 
-bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
-
-rk_status check_rows(const int64_t *targets, const int32_t *cu, int32_t num_seqs) {
-    if (!targets) return RK_ERR_INVALID_ARG;
-    if (cu && num_seqs < 0) return RK_ERR_INVALID_ARG;
-    return RK_OK;
-}
+using rk::aligned;
+using rk::check_rows;
 
 }  // namespace
 
@@ -397,6 +392,17 @@ rk_status rk_linear_logp_bwd_full(const uint16_t *h, const uint16_t *W, const in
                                    static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return rk::cuda_fail(e);
     return RK_OK;
+}
+
+rk_status rk_set_row_blocks(int32_t n) {
+    if (n < 0 || n > 2) return RK_ERR_INVALID_ARG;
+    rk::set_row_blocks_override((int)n);
+    return RK_OK;
+}
+
+int32_t rk_last_row_blocks(int32_t gemm) {
+    if (gemm != 0 && gemm != 1) return -1;
+    return (int32_t)rk::last_row_blocks(gemm == 0 ? rk::RowGemm::kDhGemm : rk::RowGemm::kDwGemm);
 }
 
 rk_status rk_selftest_wait_timeout(int64_t limit_ns, void *stream) {

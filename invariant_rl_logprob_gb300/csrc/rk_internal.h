@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "rk.h"
+
 namespace rk {
 
 // Per-device facts the launchers need (cached by rk_api.cu).
@@ -14,6 +16,17 @@ struct DeviceInfo {
     int sm_count = 0;
     unsigned *err = nullptr;  // device address of this device's error word
 };
+
+// Argument checks shared by the entry points.
+inline bool aligned(const void *p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+// targets is required; cu_seqlens, when given, needs num_seqs >= 0.
+inline rk_status check_rows(const int64_t *targets, const int32_t *cu, int32_t num_seqs) {
+    if (!targets) return RK_ERR_INVALID_ARG;
+    if (cu && num_seqs < 0) return RK_ERR_INVALID_ARG;
+    return RK_OK;
+}
 
 // Records the CUDA error behind an RK_ERR_CUDA for rk_last_cuda_error().
 void record_cuda_error(int e);
@@ -128,6 +141,14 @@ cudaError_t launch_linear_bwd_full(const uint16_t *h, const uint16_t *W, const i
                                    const float *lse, const float *grad, const int64_t *order,
                                    int64_t n, float *dh, float *dW, void *workspace,
                                    const DeviceInfo &di, cudaStream_t st);
+
+// ---- dh / dW GEMM form (linear_logp_tc.cu) ----
+// Both GEMMs run with one or two 256-row blocks per tile; the form never
+// changes a bit.  0 = automatic, 1 or 2 = forced (process-wide).
+enum class RowGemm { kDhGemm = 0, kDwGemm = 1 };
+void set_row_blocks_override(int n);
+// Blocks per tile of the last dh / dW GEMM launched on this host thread (0: none yet).
+int last_row_blocks(RowGemm which);
 
 // ---- linear_logp backward (linear_logp_tc.cu) ----
 size_t linear_bwd_chunk_bytes(int64_t rows, int64_t V);

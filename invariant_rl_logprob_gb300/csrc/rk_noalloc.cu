@@ -48,14 +48,15 @@ extern "C" rk_status rk_linear_logp_noalloc(const uint16_t *h, const uint16_t *W
                                             const int64_t *targets, const int32_t *cu_seqlens,
                                             int32_t num_seqs, int64_t T, int64_t H, int64_t V,
                                             float *logp, float *lse, void *stream) {
+    // the same checks, in the same order, as rk_linear_logp
     if (T < 0 || H <= 0 || V <= 0) return RK_ERR_INVALID_ARG;
     if (T == 0) return RK_OK;
-    if (!h || !W || !logp || !targets) return RK_ERR_INVALID_ARG;
-    if (cu_seqlens && num_seqs < 0) return RK_ERR_INVALID_ARG;
+    if (!h || !W || !logp) return RK_ERR_INVALID_ARG;
+    const rk_status st = rk::check_rows(targets, cu_seqlens, num_seqs);
+    if (st != RK_OK) return st;
     if (H % 64 != 0 || H > 65536 || V >= (int64_t(1) << 31) || T >= (int64_t(1) << 31))
         return RK_ERR_UNSUPPORTED;
-    if ((reinterpret_cast<uintptr_t>(h) & 15u) || (reinterpret_cast<uintptr_t>(W) & 15u))
-        return RK_ERR_UNSUPPORTED;
+    if (!rk::aligned(h, 16) || !rk::aligned(W, 16)) return RK_ERR_UNSUPPORTED;
     // The scratch this call needs must fit the fixed array; larger requests are
     // refused here, before anything runs.
     if (rk::linear_fwd_workspace_bytes(T, V) > kNoAllocScratchBytes) return RK_ERR_WORKSPACE;

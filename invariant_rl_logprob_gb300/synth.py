@@ -259,20 +259,23 @@ def logits_batch(T: int | None = None, V: int | None = None, seed: int | None = 
     return z.to(torch.bfloat16), targets, spike_rows
 
 
-def llama_pool(T: int | None = None) -> Pool:
+def llama_pool(T: int | None = None, with_grad: bool = False) -> Pool:
+    """The Llama-shaped workload; ``with_grad`` also draws g ~ N(0, 1) per
+    token (after h and the targets, which it leaves unchanged)."""
     c = WORKLOADS["llama"]
     T = c["T"] if T is None else T
     gen = generator(c["seed"] + 500)
     lengths = varlen_lengths(gen, T, c["len_lo"], c["len_hi"])
-    return make_pool(c["H"], c["V"], lengths, c["seed"])
+    return make_pool(c["H"], c["V"], lengths, c["seed"], with_grad=with_grad)
 
 
-def qwen_pool() -> Pool:
+def qwen_pool(with_grad: bool = False) -> Pool:
+    """The Qwen-shaped pool of 32 sequences; ``with_grad`` as for llama_pool."""
     c = WORKLOADS["qwen"]
     gen = generator(c["seed"] + 500)
     lengths = [int(torch.randint(c["len_lo"], c["len_hi"] + 1, (1,), generator=gen).item())
                for _ in range(c["pool"])]
-    return make_pool(c["H"], c["V"], lengths, c["seed"])
+    return make_pool(c["H"], c["V"], lengths, c["seed"], with_grad=with_grad)
 
 
 def grpo_pool(n_seqs: int | None = None) -> Pool:

@@ -121,3 +121,10 @@ def test_argument_errors_of_the_widened_rows(lib):
     st.restype = ctypes.c_int
     st.argtypes = [i64, vp]
     assert st(0, None) == 1 and st(20_000_000_000, None) == 1
+    # the dh / dW GEMM form: host-side setting and query only
+    sr, lr = lib.rk_set_row_blocks, lib.rk_last_row_blocks
+    sr.restype, sr.argtypes = ctypes.c_int, [i32]
+    lr.restype, lr.argtypes = i32, [i32]
+    assert sr(3) == 1 and sr(-1) == 1
+    assert sr(2) == 0 and sr(1) == 0 and sr(0) == 0
+    assert lr(0) == 0 and lr(1) == 0 and lr(2) == -1    # no GEMM launched in this thread

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from invariant_rl_logprob_gb300 import contract, synth
-from tests.helpers import DEV, bits_np, cuda, same_bits
+from tests.helpers import DEV, bits_np, cuda, oracle_bwd, oracle_dw, same_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -206,4 +206,175 @@ def test_skewed_targets(rk):
     assert chk.passed, chk
     dh2, dW2 = rk.linear_logp_bwd_full(hd, Wd, tgd, lse, gd)
     assert same_bits(dW2, dW)
+    assert rk.get_device_error() == 0
+
+
+# --------------------------------------------------------------------------
+# the paths dW and the fused backward take at full size
+# --------------------------------------------------------------------------
+
+def _zipf_targets(gen, T, V, a=1.1):
+    # seeded Zipf(a) over the vocabulary: common tokens repeat, as in real text
+    p = np.arange(1, V + 1, dtype=np.float64) ** -a
+    rng = np.random.default_rng(int(torch.randint(0, 2**31 - 1, (1,), generator=gen).item()))
+    return torch.as_tensor(rng.choice(V, size=T, p=p / p.sum()), dtype=torch.int64)
+
+
+@pytest.mark.parametrize("kind", ["uniform", "zipf", "peaked"])
+def test_dw_large_vocabulary_vs_oracle(rk, kind):
+    # V = 128256: column indices take 17 bits, so the stable column sort of
+    # the fp32 entries runs 4 radix passes of 5 bits (V <= 32768 runs at most
+    # 3), and most entries sit in columns >= 32768.  "peaked" (logit std ~5)
+    # adds a few columns per row with p >= 1/64 at random places.
+    T, H, V = 600, 256, 128256
+    h, W, tg, g = _case(T, H, V, 7100 + len(kind), w_std=0.3 if kind == "peaked" else 0.02)
+    if kind == "zipf":
+        tg = _zipf_targets(synth.generator(7200), T, V)
+    tg[::17] = -100
+    assert (tg >= 32768).sum() > (T // 4 if kind != "zipf" else 0)
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    _, lse = rk.linear_logp(hd, Wd, tgd)
+    dW = rk.linear_logp_dw(hd, Wd, tgd, lse, gd)
+    assert rk.last_row_blocks("dw") == 1            # K = 600 tokens: a short K loop
+    hb, Wb, g64 = bits_np(h), bits_np(W), g.double().numpy()
+    ref = oracle_dw(hb, Wb, tg.numpy(), g64)
+    chk = contract.check_gradient_accuracy(dW.cpu().numpy(), ref)
+    print(f"dW V=128256 {kind}: {chk}")
+    assert chk.passed, chk
+    dh2, dW2 = rk.linear_logp_bwd_full(hd, Wd, tgd, lse, gd)
+    assert same_bits(dW2, dW)
+    ref_dh = oracle_bwd(hb, Wb, tg.numpy(), g64)
+    chk = contract.check_gradient_accuracy(dh2.cpu().numpy(), ref_dh)
+    print(f"dh (full backward) V=128256 {kind}: {chk}")
+    assert chk.passed, chk
+    assert rk.get_device_error() == 0
+
+
+_LONG_K = {}
+
+
+def _long_k_reference():
+    # 16384 canonical tokens: the dW GEMM's K loop is 256 stages of 64 (the
+    # length from which the launcher takes two row blocks per tile)
+    if not _LONG_K:
+        T, H, V = 16384, 128, 4096
+        h, W, tg, g = _case(T, H, V, 7300, w_std=0.1)
+        tg[::29] = -100
+        _LONG_K["in"] = (h, W, tg, g)
+        _LONG_K["dW"] = oracle_dw(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy())
+    return _LONG_K["in"], _LONG_K["dW"]
+
+
+@pytest.mark.parametrize("blocks", [1, 2])
+def test_dw_long_token_axis_vs_oracle(rk, blocks):
+    # both GEMM forms on a 256-stage K loop, forced (the launcher alone picks
+    # two blocks only when there are also ~8 tiles per resident pair, far
+    # beyond what the oracle finishes in seconds), against the oracle and
+    # against each other bit for bit
+    (h, W, tg, g), ref = _long_k_reference()
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    _, lse = rk.linear_logp(hd, Wd, tgd)
+    rk.set_row_blocks(blocks)
+    try:
+        dW = rk.linear_logp_dw(hd, Wd, tgd, lse, gd)
+        assert rk.last_row_blocks("dw") == blocks
+        dh, dW_full = rk.linear_logp_bwd_full(hd, Wd, tgd, lse, gd)
+        assert rk.last_row_blocks("dw") == blocks and rk.last_row_blocks("dh") == blocks
+    finally:
+        rk.set_row_blocks(0)
+    chk = contract.check_gradient_accuracy(dW.cpu().numpy(), ref)
+    print(f"dW K=16384 blocks={blocks}: {chk}")
+    assert chk.passed, chk
+    assert same_bits(dW_full, dW)
+    _LONG_K.setdefault("bits", {})[blocks] = dW.cpu()
+    if len(_LONG_K["bits"]) == 2:
+        assert same_bits(_LONG_K["bits"][1], _LONG_K["bits"][2])
+    assert rk.get_device_error() == 0
+
+
+def test_dh_two_row_blocks_vs_oracle(rk):
+    # the dh GEMM's K loop is the vocabulary: V = 20000 gives 313 stages;
+    # two row blocks per tile (forced) against the oracle on every row, and
+    # bit for bit against one block
+    T, H, V = 1500, 256, 20000
+    h, W, tg, g = _case(T, H, V, 7400)
+    tg[::23] = -100
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    _, lse = rk.linear_logp(hd, Wd, tgd)
+    out = {}
+    try:
+        for blocks in (2, 1):
+            rk.set_row_blocks(blocks)
+            out[blocks] = rk.linear_logp_bwd(hd, Wd, tgd, lse, gd)
+            assert rk.last_row_blocks("dh") == blocks
+    finally:
+        rk.set_row_blocks(0)
+    assert same_bits(out[1], out[2])
+    ref = oracle_bwd(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy())
+    chk = contract.check_gradient_accuracy(out[2].cpu().numpy(), ref)
+    print(f"dh V=20000 blocks=2: {chk}")
+    assert chk.passed, chk
+    assert rk.get_device_error() == 0
+
+
+def _projection_identity(h, W, dh, dW, n_pairs=4, seed=7500):
+    """For any a, b in R^H: sum_t (h_t.a)(dh_t.b) = sum_v (W_v.b)(dW_v.a).
+
+    Both sides equal sum_{t,v} D[t,v] (h_t.a)(W_v.b) with D = dlogp/dz, since
+    dh = D W and dW = D^T h.  Returns the worst |lhs - rhs| / sum|terms|."""
+    gen = torch.Generator(device=h.device)
+    gen.manual_seed(seed)
+    worst = 0.0
+    H = h.shape[1]
+    for _ in range(n_pairs):
+        a = torch.randn(H, generator=gen, device=h.device, dtype=torch.float64)
+        b = torch.randn(H, generator=gen, device=h.device, dtype=torch.float64)
+        ha = torch.cat([h[i:i + 8192].double() @ a for i in range(0, h.shape[0], 8192)])
+        db = torch.cat([dh[i:i + 8192].double() @ b for i in range(0, dh.shape[0], 8192)])
+        wb = torch.cat([W[i:i + 8192].double() @ b for i in range(0, W.shape[0], 8192)])
+        da = torch.cat([dW[i:i + 8192].double() @ a for i in range(0, dW.shape[0], 8192)])
+        lhs, rhs = (ha * db).sum().item(), (wb * da).sum().item()
+        scale = (ha * db).abs().sum().item() + (wb * da).abs().sum().item()
+        worst = max(worst, abs(lhs - rhs) / scale)
+    return worst
+
+
+@pytest.mark.slow
+def test_grpo_full_size_dw(rk):
+    # The GRPO group itself (T = 65536, H = 4096, V = 128256): here the
+    # launcher picks two row blocks per tile for both GEMMs on its own, and
+    # the column sort runs 4 passes.  The oracle cannot compute dW at this
+    # size (every token's softmax over 128256 columns), so:
+    #  - dW of the fused backward equals rk_linear_logp_dw's and the forced
+    #    one-block form's, bit for bit;
+    #  - dh (checked against the oracle on sampled rows elsewhere) and dW
+    #    satisfy the projection identity of dh = D W, dW = D^T h;
+    #  - dW rows of vocabulary entries no token targets are -sum_t g_t p h_t
+    #    and so tiny; every value is finite.
+    pool = synth.grpo_pool()
+    h, W, tg, g = cuda(pool.h), cuda(pool.W), cuda(pool.targets), cuda(pool.g)
+    _, lse = rk.linear_logp(h, W, tg)
+    dh, dW = rk.linear_logp_bwd_full(h, W, tg, lse, g)
+    assert rk.last_row_blocks("dw") == 2 and rk.last_row_blocks("dh") == 2
+    assert torch.isfinite(dW).all() and torch.isfinite(dh).all()
+    dW_sep = rk.linear_logp_dw(h, W, tg, lse, g)
+    assert rk.last_row_blocks("dw") == 2
+    assert torch.equal(dW_sep.view(torch.int32), dW.view(torch.int32))
+    del dW_sep
+    rk.set_row_blocks(1)
+    try:
+        dW_one = rk.linear_logp_dw(h, W, tg, lse, g)
+        assert rk.last_row_blocks("dw") == 1
+    finally:
+        rk.set_row_blocks(0)
+    assert torch.equal(dW_one.view(torch.int32), dW.view(torch.int32))
+    del dW_one
+    rel = _projection_identity(h, W, dh, dW)
+    print(f"GRPO dW projection identity: worst relative residual {rel:.3g}")
+    assert rel < 1e-4, rel
+    hit = torch.zeros(pool.V, dtype=torch.bool, device=DEV)
+    hit[tg] = True
+    untargeted = dW[~hit].abs().max().item()
+    targeted = dW[hit].abs().max().item()
+    assert untargeted < 0.1 * targeted, (untargeted, targeted)
     assert rk.get_device_error() == 0

@@ -242,8 +242,9 @@ def test_logits_path_transforms(rk):
 
 @pytest.mark.slow
 def test_llama_t1_t2_t3(rk):
-    pool = synth.llama_pool()
-    runner = Runner(rk, pool, with_bwd=False)
+    # logp, lse and dh of the picked sequences, bitwise, under T1-T3
+    pool = synth.llama_pool(with_grad=True)
+    runner = Runner(rk, pool)
     n = len(pool.lengths)
     base = synth.packed(pool, list(range(n)))
     bout = runner.run(base)
@@ -263,8 +264,10 @@ def test_llama_t1_t2_t3(rk):
 
 @pytest.mark.slow
 def test_qwen_padding_vs_packing(rk):
-    pool = synth.qwen_pool()
-    runner = Runner(rk, pool, with_bwd=False)
+    # logp, lse and dh of the active tokens, bitwise: B = 8 and B = 32
+    # right-padded, B = 1 padded, against the varlen pack (T4 / T6, T1)
+    pool = synth.qwen_pool(with_grad=True)
+    runner = Runner(rk, pool)
     base = synth.packed(pool, list(range(8)))                    # varlen pack of seqs 0-7
     bout = runner.run(base)
     b8 = synth.padded(pool, list(range(8)), 2048)                # [8, 2048] right-padded
@@ -302,3 +305,34 @@ def test_grpo_decode_rows_match_prefill(rk):
                 for k in out:
                     assert torch.equal(out[k][j].view(torch.int32), bout[k][b].view(torch.int32)), \
                         (k, i, p, n_rows)
+
+
+@pytest.mark.slow
+def test_qwen_dw_padding_packing_permutation(rk):
+    # dW over the same complete sample set (the active tokens of sequences
+    # 0-7 of the Qwen-shaped pool, in canonical (sequence, position) order),
+    # from a right-padded [8, 2048] batch, a left-padded one, the varlen pack
+    # and a permuted pack behind 37 pad rows: bitwise equal (issue #244,
+    # Workstream 3, logical-workload identity).  The fused backward gives the
+    # same dW bits.
+    pool = synth.qwen_pool(with_grad=True)
+    W = cuda(pool.W)
+    seqs = list(range(8))
+
+    def dw_of(lay, full=False):
+        order = torch.tensor([r for i in seqs for r in lay.rows_of[i]], dtype=torch.int64)
+        h, tg, g = cuda(lay.h), cuda(lay.targets), cuda(lay.g)
+        _, lse = rk.linear_logp(h, W, tg)
+        if full:
+            return rk.linear_logp_bwd_full(h, W, tg, lse, g, row_order=cuda(order))[1]
+        return rk.linear_logp_dw(h, W, tg, lse, g, row_order=cuda(order))
+
+    base = dw_of(synth.packed(pool, seqs)).cpu()
+    assert torch.isfinite(base).all()
+    for lay, full in ((synth.padded(pool, seqs, 2048, side="right"), False),
+                      (synth.padded(pool, seqs, 2048, side="left"), False),
+                      (synth.packed(pool, [7, 3, 5, 1, 0, 6, 2, 4], lead_pad=37), False),
+                      (synth.padded(pool, seqs, 2048, side="right"), True)):
+        got = dw_of(lay, full).cpu()
+        assert torch.equal(got.view(torch.int32), base.view(torch.int32)), (lay.description, full)
+    assert rk.get_device_error() == 0

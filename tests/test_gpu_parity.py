@@ -138,10 +138,11 @@ def test_llama_shape_sampled_rows(rk):
     pool = synth.llama_pool()
     lay = synth.packed(pool, list(range(len(pool.lengths))))
     logp, lse = rk.linear_logp(cuda(lay.h), cuda(pool.W), cuda(lay.targets), cuda(lay.cu_seqlens))
-    rows = synth.sample_rows(lay.T, 64, seed=2)
+    rows = synth.sample_rows(lay.T, 256, seed=2)
     ref_logp, ref_lse = oracle_linear(bits_np(lay.h), bits_np(pool.W), lay.targets.numpy(),
                                       lay.cu_seqlens.numpy(), rows=rows)
-    _check_fwd(logp.cpu()[rows], lse.cpu()[rows], ref_logp, ref_lse, "llama sampled")
+    c1, c2 = _check_fwd(logp.cpu()[rows], lse.cpu()[rows], ref_logp, ref_lse, "llama sampled")
+    print(f"llama 256 sampled rows: logp {c1}; lse {c2}")
     # properties at full size: logp <= 0 on every active row, all finite
     lp = logp.cpu()
     assert torch.all(torch.isfinite(lp)) and torch.all(lp <= 0)
@@ -348,12 +349,16 @@ def test_grpo_shape_sampled_rows(rk):
     h, W, tg, g = cuda(lay.h), cuda(pool.W), cuda(lay.targets), cuda(lay.g)
     logp, lse = rk.linear_logp(h, W, tg)
     dh = rk.linear_logp_bwd(h, W, tg, lse, g)
-    rows = synth.sample_rows(lay.T, 16, seed=4)
+    # the launch the bench times: one pass over all rows, two row blocks per
+    # dh tile (K = 2004 stages of the vocabulary)
+    assert rk.last_row_blocks("dh") == 2
+    rows = synth.sample_rows(lay.T, 64, seed=4)
     hb, Wb = bits_np(lay.h), bits_np(pool.W)
     ref_logp, ref_lse = oracle_linear(hb, Wb, lay.targets.numpy(), rows=rows)
-    _check_fwd(logp.cpu()[rows], lse.cpu()[rows], ref_logp, ref_lse, "grpo fwd sampled")
+    c1, c2 = _check_fwd(logp.cpu()[rows], lse.cpu()[rows], ref_logp, ref_lse, "grpo fwd sampled")
     ref_dh = oracle_bwd(hb, Wb, lay.targets.numpy(), lay.g.double().numpy(), rows=rows)
-    _check_bwd(dh.cpu()[rows], ref_dh, "grpo bwd sampled")
+    c3 = _check_bwd(dh.cpu()[rows], ref_dh, "grpo bwd sampled")
+    print(f"grpo 64 sampled rows: logp {c1}; lse {c2}; dh {c3}")
     assert rk.get_device_error() == 0
 
 

@@ -79,6 +79,27 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
     assert rk.get_device_error() == 0
 
 
+def test_noalloc_allocates_no_device_memory(lib):
+    # After one warm-up call (which looks up the array's address and loads
+    # the kernels), further calls of other shapes leave both the driver's
+    # free-memory count and PyTorch's allocator exactly where they were.
+    h, W, tg, cu = workload(2048, 256, 50000, seed=93, varlen=True)
+    h2, W2, tg2, _ = workload(700, 512, 9000, seed=94)
+    logp = torch.empty(2048, dtype=torch.float32, device=h.device)
+    lse = torch.empty(2048, dtype=torch.float32, device=h.device)
+    assert call_noalloc(lib, h, W, tg, cu, logp, lse) == RK_OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0, reserved0 = torch.cuda.memory_allocated(), torch.cuda.memory_reserved()
+    for _ in range(3):
+        assert call_noalloc(lib, h2, W2, tg2, None, logp[:700], lse[:700]) == RK_OK
+        assert call_noalloc(lib, h, W, tg, cu, logp, lse) == RK_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert torch.cuda.memory_allocated() == alloc0 and torch.cuda.memory_reserved() == reserved0
+
+
 def test_noalloc_refuses_requests_beyond_its_scratch(lib):
     # V = 128256: 8363 rows fit in 32 MiB, 8364 do not
     import invariant_rl_logprob_gb300 as rk
