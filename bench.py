@@ -42,6 +42,7 @@ UNIT = "tokens/s"
 GRPO = dict(n_seqs=64, seq_len=1024, H=4096, V=128256)
 LOGITS = dict(T=2048, V=32000)
 N_LOGITS_BUFFERS = 4
+LOGITS_REPEATS = 7
 WORKLOAD = ("grpo_fwd_bwd: linear_logp fwd+bwd T=65536 (64x1024) H=4096 V=128256 bf16, "
             "+ logits path T=2048 V=32000 bf16")
 
@@ -256,6 +257,21 @@ def hold_stream(stream, ms: float = 5.0) -> None:
         torch.cuda._sleep(int(ms * 2.1e6))
 
 
+def sm_clock_mhz(stream) -> float:
+    """The SM clock right now, measured on the device: a spin of a known
+    number of SM cycles (torch.cuda._sleep) timed with CUDA events."""
+    import torch
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    cycles = 1_000_000
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        torch.cuda._sleep(cycles)
+        b.record(stream)
+    b.synchronize()
+    return cycles / (a.elapsed_time(b) * 1e3)
+
+
 def time_loop(fn, reps: int, stream) -> float:
     """Mean device ms per call of `fn` over `reps` back-to-back calls (after 3
     warm-up calls; the calls are queued behind a device-side wait so that
@@ -371,6 +387,52 @@ def measure_rows(rk, pool, zs, peaks, dev, stream) -> dict:
                                    "frac": tf / peaks["bf16_tflops_sustained"],
                                    "algorithmic": "6*T*H*V flop (dZ + dh + dW GEMMs)"}
     del wsd, dW, dh
+    out.update(measure_config_rows(rk, peaks, dev, stream))
+    return out
+
+
+def measure_config_rows(rk, peaks, dev, stream) -> dict:
+    """linear_logp forward on the Llama- and Qwen-shaped workloads: tokens/s
+    and the fraction of the burst bf16 rate (each a loop of a few calls), with
+    the work counted on active tokens only (2*H*V flop per active token)."""
+    import torch
+
+    from invariant_rl_logprob_gb300 import synth
+    out = {}
+
+    def fwd_row(lay, W, n_calls):
+        h, tg = lay.h.to(dev), lay.targets.to(dev)
+        cu = lay.cu_seqlens.to(dev) if lay.cu_seqlens is not None else None
+        T, H, V = h.shape[0], h.shape[1], W.shape[0]
+        act = lay.targets >= 0
+        if lay.cu_seqlens is not None:
+            r = torch.arange(T)
+            act &= (r >= int(lay.cu_seqlens[0])) & (r < int(lay.cu_seqlens[-1]))
+        n_act = int(act.sum())
+        ws = torch.empty(rk.linear_logp_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
+        logp = torch.empty(T, dtype=torch.float32, device=dev)
+        lse = torch.empty(T, dtype=torch.float32, device=dev)
+        ms = time_loop(lambda i: rk.linear_logp(h, W, tg, cu, out=logp, lse=lse, workspace=ws,
+                                                stream=stream), n_calls, stream)
+        tf = 2.0 * n_act * H * V / (ms / 1e3) / 1e12
+        return {"rows": T, "active_tokens": n_act, "H": H, "V": V, "ms_per_call": ms,
+                "active_tokens_per_s": n_act / (ms / 1e3), "bound": "tensor", "achieved": tf,
+                "unit": "TFLOP/s", "peak": peaks["bf16_tflops"],
+                "frac": tf / peaks["bf16_tflops"], "peak_source": "burst bf16",
+                "algorithmic": "2*H*V flop per active token"}
+
+    pool = synth.llama_pool()
+    W = pool.W.to(dev)
+    lay = synth.packed(pool, list(range(len(pool.lengths))))
+    out["llama_fwd_varlen"] = fwd_row(lay, W, 10)
+    out["llama_fwd_varlen"]["sequences"] = len(pool.lengths)
+    del W, pool, lay
+    pool = synth.qwen_pool()
+    W = pool.W.to(dev)
+    out["qwen_fwd_padded_b8"] = fwd_row(synth.padded(pool, list(range(8)), 2048), W, 10)
+    out["qwen_fwd_packed_seqs0_7"] = fwd_row(synth.packed(pool, list(range(8))), W, 10)
+    del W, pool
+    torch.cuda.empty_cache()
     return out
 
 
@@ -456,22 +518,28 @@ def run_gpu(args) -> None:
     if err:
         raise RuntimeError(f"device error word {err:#x} in the timed region")
 
-    # the logits path on its own: a loop over the rotated buffers (each call's
-    # input is absent from L2, and no dirty lines of the GEMMs are pending)
+    # the logits path on its own: loops over the rotated buffers (each call's
+    # input is absent from L2), repeated right after the step loop, while the
+    # SM clock is still recovering from the power-capped GEMMs, and on; each
+    # repeat carries the SM clock measured on the device around it
     lg_reps = 50
-    for i in range(3):
-        z, zt = zs[i % len(zs)]
-        rk.logp_from_logits(z, zt, out=zlogp, lse=zlse, stream=stream)
-    ls0 = torch.cuda.Event(enable_timing=True)
-    ls1 = torch.cuda.Event(enable_timing=True)
-    hold_stream(stream, 5.0)
-    ls0.record(stream)
-    for i in range(lg_reps):
-        z, zt = zs[i % len(zs)]
-        rk.logp_from_logits(z, zt, out=zlogp, lse=zlse, stream=stream)
-    ls1.record(stream)
+    lg_runs = []
+    for r in range(LOGITS_REPEATS):
+        f0 = sm_clock_mhz(stream)
+        ls0 = torch.cuda.Event(enable_timing=True)
+        ls1 = torch.cuda.Event(enable_timing=True)
+        hold_stream(stream, 2.0)
+        ls0.record(stream)
+        for i in range(lg_reps):
+            z, zt = zs[i % len(zs)]
+            rk.logp_from_logits(z, zt, out=zlogp, lse=zlse, stream=stream)
+        ls1.record(stream)
+        f1 = sm_clock_mhz(stream)
+        lg_runs.append({"us_per_call": ls0.elapsed_time(ls1) * 1000.0 / lg_reps,
+                        "sm_mhz_before": round(f0), "sm_mhz_after": round(f1)})
     torch.cuda.synchronize(dev)
-    lg_loop_ms = ls0.elapsed_time(ls1) / lg_reps
+    lg_us = sorted(r["us_per_call"] for r in lg_runs)
+    lg_loop_ms = statistics.median(lg_us) / 1000.0
 
     ms_step_local = total_ms / args.steps
     ms_step = max_over_ranks(ms_step_local, ws)
@@ -617,9 +685,14 @@ def run_gpu(args) -> None:
                         "unit": "GB/s", "frac": lg_gbs / peaks["hbm_gbs"],
                         "bytes_per_call": lg_bytes, "us_per_call": lg_loop_ms * 1000.0,
                         "tokens_per_s": Tl / (lg_loop_ms / 1000.0),
-                        "timing": f"{lg_reps} back-to-back calls over {N_LOGITS_BUFFERS} rotated "
-                                  "buffers after the step loop (CUDA events on the launching "
-                                  "stream; queued behind a device-side wait)",
+                        "us_per_call_min_median_max": [lg_us[0], statistics.median(lg_us),
+                                                       lg_us[-1]],
+                        "repeats": lg_runs,
+                        "timing": f"median of {LOGITS_REPEATS} loops of {lg_reps} back-to-back "
+                                  f"calls over {N_LOGITS_BUFFERS} rotated buffers, the first "
+                                  "right after the step loop (CUDA events on the launching "
+                                  "stream; queued behind a device-side wait); SM clock measured "
+                                  "on the device before and after each loop",
                         "in_step": {"us_per_call": lg_ms * 1000.0, "achieved": lg_gbs_step,
                                     "frac": lg_gbs_step / peaks["hbm_gbs"],
                                     "note": "measured right after the dh GEMM: its dirty L2 "

@@ -222,6 +222,30 @@ rk_status rk_grpo_token_loss(const float *logp, const float *logp_old, const flo
                              void *stream);
 
 /*
+ * rk_linear_logp followed by rk_grpo_token_loss on its logp, in one call: the
+ * forward's final merge applies the per-token loss to each logp it has just
+ * produced, so the logprobs never make a second trip through memory and one
+ * launch is saved.  Every output (logp, lse, loss, grad_logp, ratio, kl) is
+ * bitwise identical to the two separate calls on the same inputs.
+ *   h, W, targets, cu_seqlens, num_seqs, T, H, V, logp, lse, workspace,
+ *   workspace_bytes: as for rk_linear_logp (workspace >=
+ *   rk_linear_logp_workspace_size(T, H, V));
+ *   logp_old, logp_ref, advantages, eps_low, eps_high, beta, scale, loss,
+ *   grad_logp, ratio, kl: as for rk_grpo_token_loss.
+ * Rows whose target is >= V get NaN logp, and the loss arithmetic then runs on
+ * that NaN, as it would in the separate call.
+ */
+rk_status rk_linear_logp_grpo(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                              const int32_t *cu_seqlens, int32_t num_seqs,
+                              int64_t T, int64_t H, int64_t V,
+                              const float *logp_old, const float *logp_ref,
+                              const float *advantages, float eps_low, float eps_high,
+                              float beta, float scale,
+                              float *logp, float *lse, float *loss, float *grad_logp,
+                              float *ratio, float *kl,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Greedy decoding step fused with its selected logprob: for every row (rows
  * outside [cu_seqlens[0], cu_seqlens[num_seqs]) when cu_seqlens is given get
  * token -1 and logp = lse = 0),

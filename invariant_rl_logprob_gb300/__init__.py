@@ -27,7 +27,7 @@ __all__ = [
     "linear_logp", "linear_logp_workspace_size",
     "logp_from_logits",
     "linear_logp_bwd", "linear_logp_bwd_workspace_size", "linear_logp_bwd_min_workspace_size",
-    "lm_head", "logp_from_logits_bwd", "grpo_token_loss", "linear_greedy",
+    "lm_head", "logp_from_logits_bwd", "grpo_token_loss", "linear_logp_grpo", "linear_greedy",
     "linear_greedy_workspace_size", "linear_logp_dw", "linear_logp_dw_workspace_size",
     "linear_logp_bwd_full", "linear_logp_bwd_full_workspace_size", "lm_head_workspace_size",
     "get_device_error", "selftest_wait_timeout", "set_row_blocks", "last_row_blocks", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT", "DEVERR_LSE",
@@ -115,6 +115,10 @@ def load_library() -> ctypes.CDLL:
     lib.rk_last_cuda_error.restype = ctypes.c_int
     lib.rk_version.argtypes = []
     lib.rk_version.restype = ctypes.c_char_p
+    f32 = ctypes.c_float
+    lib.rk_linear_logp_grpo.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, f32, f32,
+                                        f32, f32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.rk_linear_logp_grpo.restype = ctypes.c_int
     lib.rk_set_row_blocks.argtypes = [i32]
     lib.rk_set_row_blocks.restype = ctypes.c_int
     lib.rk_last_row_blocks.argtypes = [i32]
@@ -323,6 +327,43 @@ def grpo_token_loss(logp: torch.Tensor, logp_old: torch.Tensor, advantages: torc
                                 _ptr(out["loss"]), _ptr(out["grad"]), _ptr(out["ratio"]),
                                 _ptr(out["kl"]), _stream_handle(stream, logp.device))
     _check(st, "rk_grpo_token_loss")
+    return out
+
+
+def linear_logp_grpo(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor,
+                     logp_old: torch.Tensor, advantages: torch.Tensor,
+                     cu_seqlens: torch.Tensor | None = None, *,
+                     logp_ref: torch.Tensor | None = None, eps_low: float = 0.2,
+                     eps_high: float = 0.2, beta: float = 0.0, scale: float = 1.0,
+                     workspace: torch.Tensor | None = None,
+                     stream: torch.cuda.Stream | None = None) -> dict:
+    """linear_logp with the per-token GRPO loss applied in its merge: dict of
+    fp32 ``[T]`` tensors ``logp``, ``lse``, ``loss``, ``grad``, ``ratio``,
+    ``kl`` (the same bits as linear_logp followed by grpo_token_loss)."""
+    lib = load_library()
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    T, H = h.shape
+    V = W.shape[0]
+    if W.shape[1] != H or W.device != h.device:
+        raise ValueError("W must be [V, H] on h's device")
+    for name, t in (("logp_old", logp_old), ("advantages", advantages)):
+        _need(t, name, torch.float32, 1)
+    if logp_ref is not None:
+        _need(logp_ref, "logp_ref", torch.float32, 1)
+    cu, ns = _rows(targets, cu_seqlens, T, h.device)
+    out = {k: torch.empty(T, dtype=torch.float32, device=h.device)
+           for k in ("logp", "lse", "loss", "grad", "ratio", "kl")}
+    need = int(lib.rk_linear_logp_workspace_size(T, H, V))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
+    st = lib.rk_linear_logp_grpo(_ptr(h), _ptr(W), _ptr(targets), _ptr(cu), ns, T, H, V,
+                                 _ptr(logp_old), _ptr(logp_ref), _ptr(advantages), eps_low,
+                                 eps_high, beta, scale, _ptr(out["logp"]), _ptr(out["lse"]),
+                                 _ptr(out["loss"]), _ptr(out["grad"]), _ptr(out["ratio"]),
+                                 _ptr(out["kl"]), _ptr(workspace), workspace.numel(),
+                                 _stream_handle(stream, h.device))
+    _check(st, "rk_linear_logp_grpo")
     return out
 
 

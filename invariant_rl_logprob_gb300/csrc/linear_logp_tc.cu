@@ -62,6 +62,7 @@
 
 #include "rk_device.cuh"
 #include "rk_internal.h"
+#include "token_loss.cuh"
 
 namespace rk {
 namespace {
@@ -935,11 +936,14 @@ __device__ __forceinline__ void fold_tiles(const float2 *__restrict__ pr, int nu
     }
 }
 
+// With LOSS, the row's per-token GRPO loss (token_loss.cuh) is applied to the
+// logp just computed, exactly as rk_grpo_token_loss would apply it.
+template <bool LOSS>
 __global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
     linear_logp_merge(const float2 *__restrict__ part, const float *__restrict__ ztgt,
                       const int64_t *__restrict__ targets, const int32_t *__restrict__ cu,
                       int num_seqs, int64_t T, int32_t V, int32_t num_n, float *__restrict__ logp,
-                      float *__restrict__ lse, unsigned *err) {
+                      float *__restrict__ lse, unsigned *err, GrpoArgs loss) {
     const int64_t row = (int64_t)blockIdx.x * kMergeRowsPerBlock + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= T) return;
@@ -948,6 +952,7 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
         if (lane == 0) {
             logp[row] = 0.f;
             if (lse) lse[row] = 0.f;
+            if constexpr (LOSS) grpo_token_inactive(loss, row);
         }
         return;
     }
@@ -956,6 +961,7 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
             logp[row] = __int_as_float(0x7fc00000);
             if (lse) lse[row] = __int_as_float(0x7fc00000);
             atomicOr(err, kErrTargetRange);
+            if constexpr (LOSS) grpo_token(loss, row, __int_as_float(0x7fc00000));
         }
         return;
     }
@@ -963,8 +969,10 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
     fold_tiles(part + row * num_n, num_n, lane, m, s);
     if (lane == 0) {
         const float l = __fadd_rn(m, logf(s));
-        logp[row] = __fsub_rn(ztgt[row], l);
+        const float lp = __fsub_rn(ztgt[row], l);
+        logp[row] = lp;
         if (lse) lse[row] = l;
+        if constexpr (LOSS) grpo_token(loss, row, lp);
     }
 }
 
@@ -1128,7 +1136,7 @@ size_t linear_fwd_workspace_bytes(int64_t T, int64_t V) {
 cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
                               const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
                               float *logp, float *lse, void *workspace, const DeviceInfo &di,
-                              cudaStream_t st) {
+                              cudaStream_t st, const GrpoArgs *loss) {
     if (T == 0) return cudaSuccess;
     CUtensorMap tmA, tmB;
     if (!encode_tmap_bf16_2d(&tmA, h, (uint64_t)H, (uint64_t)T, (uint64_t)H * 2, BK, BM, true))
@@ -1157,9 +1165,12 @@ cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_
     if (e != cudaSuccess) return e;
 
     const unsigned mgrid = (unsigned)((T + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock);
-    linear_logp_merge<<<mgrid, 32 * kMergeRowsPerBlock, 0, st>>>(a.part, a.ztgt, targets, cu,
-                                                                  num_seqs, T, a.V, a.num_n, logp,
-                                                                  lse, di.err);
+    if (loss)
+        linear_logp_merge<true><<<mgrid, 32 * kMergeRowsPerBlock, 0, st>>>(
+            a.part, a.ztgt, targets, cu, num_seqs, T, a.V, a.num_n, logp, lse, di.err, *loss);
+    else
+        linear_logp_merge<false><<<mgrid, 32 * kMergeRowsPerBlock, 0, st>>>(
+            a.part, a.ztgt, targets, cu, num_seqs, T, a.V, a.num_n, logp, lse, di.err, GrpoArgs{});
     return cudaGetLastError();
 }
 

@@ -1,35 +1,45 @@
 // logits_logp.cu -- the logits path: selected-token logprob from materialised
 // bf16 logits ("logp / batch_invariant_logp", RL-Kernel issue #101, maintainer
 // comment, P0 operator list; chain index 8 of PR #264 "docs(ws1):
-// batch-invariance contract RFC").
+// batch-invariance contract RFC"), and its backward.
 //
 //   lse[t]  = log sum_v exp(logits[t, v])
 //   logp[t] = logits[t, targets[t]] - lse[t]
 //
 // HBM-bound: every logit is read once (T*V*2 bytes), nothing else is large.
 //
-// Batch invariance by construction.  A row is reduced by two warps, i.e. 64
+// Batch invariance by construction.  A row is reduced by four warps, i.e. 128
 // "virtual lanes" vl = 32 * (warp of the row) + lane.  The columns are cut into
 // groups of 8 (group g = columns [8g, 8g+8)); virtual lane vl owns groups
-// vl, vl + 64, vl + 128, ... and folds them, in that order, in batches of 8
+// vl, vl + 128, vl + 256, ... and folds them, in that order, in batches of 8
 // groups: the batch maximum (exact, any order) updates the running max once,
 // then the batch's 64 terms 2^((z - m) log2 e) are summed by a fixed pairwise
 // tree and added to the running sum.  The 32 partials of a warp are merged by a
-// fixed xor-shuffle tree, and the two warps' partials by one final merge.  All
-// of that depends only on V -- never on T, the row's index, the grid or the
+// fixed xor-shuffle tree, and the four warps' partials in warp order.  All of
+// that depends only on V -- never on T, the row's index, the grid or the
 // row's address: rows whose address allows 16-byte loads use them, others load
 // 2-byte elements into the same groups (missing columns read as -inf) and run
 // exactly the same floating-point operations.
+//
+// Four warps per row rather than fewer: with 64 values in flight per lane and
+// one wave of rows, the extra warps hide the load latency behind the other
+// warps' arithmetic, so the kernel stays at the memory's pace when the SM
+// clock drops (about 1.5 GHz right after power-capped GEMMs: 24.3 us per
+// T = 2048, V = 32000 call against 28.6 us with two warps per row).
 #include "rk_device.cuh"
 #include "rk_internal.h"
 
 namespace rk {
 namespace {
 
-constexpr int kWarpsPerRow = 2;
+// forward: four warps per row; backward: two (each element is independent)
+constexpr int kWarpsPerRow = 4;
 constexpr int kLanesPerRow = 32 * kWarpsPerRow;
 constexpr int kThreads = 128;
 constexpr int kRowsPerBlock = kThreads / kLanesPerRow;
+constexpr int kBwdWarpsPerRow = 2;
+constexpr int kBwdLanesPerRow = 32 * kBwdWarpsPerRow;
+constexpr int kBwdRowsPerBlock = kThreads / kBwdLanesPerRow;
 constexpr int kBatch = 8;  // groups per batch (64 values)
 constexpr uint32_t kNegInfPair = 0xFF80FF80u;  // two bf16 -inf
 
@@ -188,8 +198,8 @@ __global__ void __launch_bounds__(kThreads)
     wait_prior_grid();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int vl = (warp % kWarpsPerRow) * 32 + lane;
-    const int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + warp / kWarpsPerRow;
+    const int vl = (warp % kBwdWarpsPerRow) * 32 + lane;
+    const int64_t row = (int64_t)blockIdx.x * kBwdRowsPerBlock + warp / kBwdWarpsPerRow;
     if (row >= T) return;
     const int64_t tgt = targets[row];
     const bool active = row_active(row, tgt, cu, num_seqs);
@@ -203,7 +213,7 @@ __global__ void __launch_bounds__(kThreads)
     float *orow = dlogits + row * V;
     const int64_t G = (V + 7) >> 3;
 #pragma unroll 4
-    for (int64_t gi = vl; gi < G; gi += kLanesPerRow) {
+    for (int64_t gi = vl; gi < G; gi += kBwdLanesPerRow) {
         const int64_t c0 = gi << 3;
         float z[8];
         if (VEC) {
@@ -265,7 +275,7 @@ cudaError_t launch_logits_bwd(const uint16_t *logits, const int64_t *targets, co
                               const float *grad, float *dlogits, const DeviceInfo &di,
                               cudaStream_t st) {
     if (T == 0) return cudaSuccess;
-    const unsigned grid = (unsigned)((T + kRowsPerBlock - 1) / kRowsPerBlock);
+    const unsigned grid = (unsigned)((T + kBwdRowsPerBlock - 1) / kBwdRowsPerBlock);
     // VEC: 16-byte loads and 32-byte stores (rows of V % 8 == 0 elements keep
     // both aligned)
     const bool vec = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0) &&

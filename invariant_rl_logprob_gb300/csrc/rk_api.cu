@@ -9,6 +9,7 @@
 #include "rk.h"
 #include "rk_device.cuh"
 #include "rk_internal.h"
+#include "token_loss.cuh"
 
 // One error word per device (the module is loaded per device context).
 __device__ unsigned int g_rk_device_error = 0u;
@@ -170,6 +171,38 @@ rk_status rk_linear_logp(const uint16_t *h, const uint16_t *W, const int64_t *ta
     if (e != cudaSuccess) return rk::cuda_fail(e);
     e = rk::launch_linear_fwd(h, W, targets, cu_seqlens, num_seqs, T, H, V, logp, lse, workspace,
                               di, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    return RK_OK;
+}
+
+rk_status rk_linear_logp_grpo(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                              const int32_t *cu_seqlens, int32_t num_seqs, int64_t T, int64_t H,
+                              int64_t V, const float *logp_old, const float *logp_ref,
+                              const float *advantages, float eps_low, float eps_high, float beta,
+                              float scale, float *logp, float *lse, float *loss, float *grad_logp,
+                              float *ratio, float *kl, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+    if (T < 0 || H <= 0 || V <= 0) return RK_ERR_INVALID_ARG;
+    if (T == 0) return RK_OK;
+    if (!h || !W || !logp || !logp_old || !advantages || !loss || !grad_logp)
+        return RK_ERR_INVALID_ARG;
+    rk_status st = check_rows(targets, cu_seqlens, num_seqs);
+    if (st != RK_OK) return st;
+    if (!(eps_low >= 0.f && eps_low < 1.f) || !(eps_high >= 0.f) || !(beta >= 0.f))
+        return RK_ERR_INVALID_ARG;
+    if (H % 64 != 0 || H > 65536 || V >= (int64_t(1) << 31) || T >= (int64_t(1) << 31))
+        return RK_ERR_UNSUPPORTED;
+    if (!aligned(h, 16) || !aligned(W, 16)) return RK_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < rk::linear_fwd_workspace_bytes(T, V))
+        return RK_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return RK_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    const rk::GrpoArgs p{logp_old, logp_ref, advantages, eps_low, eps_high, beta, scale,
+                         loss, grad_logp, ratio, kl};
+    e = rk::launch_linear_fwd(h, W, targets, cu_seqlens, num_seqs, T, H, V, logp, lse, workspace,
+                              di, static_cast<cudaStream_t>(stream), &p);
     if (e != cudaSuccess) return rk::cuda_fail(e);
     return RK_OK;
 }

@@ -50,11 +50,13 @@ cudaError_t launch_logits_logp(const uint16_t *logits, const int64_t *targets, c
                                const DeviceInfo &di, cudaStream_t st);
 
 // ---- linear_logp forward (linear_logp_tc.cu) ----
+struct GrpoArgs;  // token_loss.cuh
 size_t linear_fwd_workspace_bytes(int64_t T, int64_t V);
+// With `loss`, the merge also applies the per-token GRPO loss to each logp.
 cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
                               const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
                               float *logp, float *lse, void *workspace, const DeviceInfo &di,
-                              cudaStream_t st);
+                              cudaStream_t st, const GrpoArgs *loss = nullptr);
 
 // ---- greedy step and dense lm_head (linear_logp_tc.cu) ----
 size_t linear_greedy_workspace_bytes(int64_t T, int64_t V);
