@@ -1,17 +1,23 @@
 """Throughput benchmark of the batch-invariant selected-token logprob path.
 
 One step = one pass of the whole hot path on one GPU:
-  1. linear_logp forward (tile kernel + merge) on a GRPO group: 64 completions
-     x 1024 tokens (T = 65536), H = 4096, V = 128256, bf16, seeded synthetic data;
-  2. linear_logp backward (dZ GEMM + dh GEMM) on the same rows, g ~ N(0, 1);
+  1. linear_logp forward on a GRPO group: 64 completions x 1024 tokens
+     (T = 65536), H = 4096, V = 128256, bf16, seeded synthetic data; the
+     forward keeps its per-tile softmax terms (bf16) for the backward
+     (rk_linear_logp_fwd_saved: tile kernel + merge);
+  2. linear_logp backward on the same rows, g ~ N(0, 1), from those terms
+     (rk_linear_logp_bwd_saved: the terms become dZ in one HBM-bound pass,
+     the target and p >= 1/64 columns get exact fp32 weights, dh GEMM);
   3. the logits path on T = 2048 rows of V = 32000 bf16 logits (rotated over 4
      buffers so that no call finds its input in L2).
+The backward that recomputes z with a second GEMM instead (rk_linear_logp +
+rk_linear_logp_bwd) is timed as its own row.
 `value` = tokens (rows of the GRPO group, summed over ranks) per second of
 device time, inputs resident in HBM.  h (512 MB) and W (1.05 GB) exceed the
 126 MB L2, so nothing carries over between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-    python bench.py --case {fwd,bwd,dw,full,logits,logits_bwd} [--shape T,H,V] [--reps R]
+    python bench.py --case {fwd,bwd,dw,full,saved,logits,logits_bwd} [--shape T,H,V] [--reps R]
 
 `--case` runs one operator a few times on a small workload (for profiler
 captures; default T=2048, H=4096, V=32000: W and the logits exceed L2) and
@@ -46,24 +52,28 @@ LOGITS_REPEATS = 7
 WORKLOAD = ("grpo_fwd_bwd: linear_logp fwd+bwd T=65536 (64x1024) H=4096 V=128256 bf16, "
             "+ logits path T=2048 V=32000 bf16")
 
-# ncu dram__bytes_read.sum + dram__bytes_write.sum of the three tile-kernel
-# launches of one step (forward, dZ GEMM, dh GEMM) on this very workload
-# (`ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
-#  --clock-control none -k regex:linear_logp_tiles -c 3 python bench.py --steps 3
-#  --warmup 3 --no-cpu-baseline --no-rows`, one pass per launch), recorded with
-# the SHA-1 of the kernel source; reported only while the source still matches.
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of the two tile-kernel
+# launches of one step (the forward that keeps its softmax terms, the dh GEMM)
+# on this very workload (`ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,
+# gpu__time_duration.sum --clock-control none -k regex:linear_logp_tiles -c 2
+# python bench.py --steps 3 --warmup 3 --no-cpu-baseline --no-rows`, one pass per
+# launch), recorded with the SHA-1 of the kernel source; reported only while the
+# source still matches.
 TRAFFIC_RECORD = {
-    "source_sha1": "8663de08b4ef2455b2772da1707943854d8bedb6",
-    "bytes_per_step": 160388734976,
-    "per_launch_gb": {"fwd": 18.79, "dZ": 36.77, "dh": 104.83},
+    "source_sha1": "",
+    "bytes_per_step": None,
+    "per_launch_gb": {},
 }
-# Unique bytes a step has to move: forward h + W + partials; dZ GEMM h + W +
-# dZ written; dh GEMM dZ + W read, dh written.
+# Unique bytes a step has to move: forward h + W read, partials + target
+# logits + the softmax terms (T*V bf16) written; stash -> dZ pass: the terms
+# read and dZ written in place, partials read; dh GEMM: dZ + W read, dh
+# written.
 def algorithmic_bytes_per_step(T: int, H: int, V: int) -> int:
     nt = (V + 255) // 256
     h, w = T * H * 2, V * H * 2
     dz = T * V * 2
-    return (h + w + T * nt * 8 + T * 4) + (h + w + dz) + (dz + w + T * H * 4)
+    part = T * nt * 8
+    return (h + w + part + T * 4 + dz) + (2 * dz + part) + (dz + w + T * H * 4)
 
 
 def kernel_source_sha1() -> str:
@@ -387,6 +397,26 @@ def measure_rows(rk, pool, zs, peaks, dev, stream) -> dict:
                                    "frac": tf / peaks["bf16_tflops_sustained"],
                                    "algorithmic": "6*T*H*V flop (dZ + dh + dW GEMMs)"}
     del wsd, dW, dh
+    # the backward that recomputes z with a second GEMM (no saved terms):
+    # forward + backward, 6*T*H*V flop
+    wsf = torch.empty(rk.linear_logp_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(rk.linear_logp_bwd_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
+    lp = torch.empty(T, dtype=torch.float32, device=dev)
+    ls = torch.empty(T, dtype=torch.float32, device=dev)
+    dh = torch.empty((T, H), dtype=torch.float32, device=dev)
+    g1 = torch.randn(T, device=dev)
+
+    def recompute_step(i):
+        rk.linear_logp(h, W, tg, out=lp, lse=ls, workspace=wsf, stream=stream)
+        rk.linear_logp_bwd(h, W, tg, ls, g1, dh=dh, workspace=wsb, stream=stream)
+    ms = time_loop(recompute_step, 3, stream)
+    tf = 6.0 * T * H * V / (ms / 1e3) / 1e12
+    out["linear_logp_fwd_bwd_recompute"] = {
+        "shape": [T, H, V], "ms_per_call": ms, "tokens_per_s": T / (ms / 1e3), "bound": "tensor",
+        "achieved": tf, "unit": "TFLOP/s", "peak": peaks["bf16_tflops_sustained"],
+        "frac": tf / peaks["bf16_tflops_sustained"],
+        "algorithmic": "6*T*H*V flop (fwd, z recompute, dZ.W)"}
+    del wsf, wsb, dh
     out.update(measure_config_rows(rk, peaks, dev, stream))
     return out
 
@@ -470,14 +500,22 @@ def run_gpu(args) -> None:
     dh = torch.empty((T, H), dtype=torch.float32, device=dev)
     zlogp = torch.empty(Tl, dtype=torch.float32, device=dev)
     zlse = torch.empty(Tl, dtype=torch.float32, device=dev)
-    ws_fwd = torch.empty(rk.linear_logp_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
-    ws_bwd = torch.empty(rk.linear_logp_bwd_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
-    bwd_chunks = 1   # the full workspace holds every row: one dZ GEMM + one dh GEMM
-    launches_per_step = 2 + (2 * bwd_chunks + 1) + 1   # fwd: 2, bwd: 3, logits: 1
+    saved = torch.empty(rk.linear_logp_saved_size(T, H, V), dtype=torch.uint8, device=dev)
+    ws_bwd = torch.empty(rk.linear_logp_bwd_saved_workspace_size(T, H, V), dtype=torch.uint8,
+                         device=dev)
+    # fwd: tile kernel + merge; bwd: stash -> dZ, exact entries, entry sort,
+    # dh tile kernel, bad-target rows; logits: 1
+    launches_per_step = 2 + 5 + 1
+
+    def fwd(hh, tt, lp, ls):
+        rk.linear_logp_fwd_saved(hh, W, tt, out=lp, lse=ls, saved=saved, stream=stream)
+
+    def bwd(hh, tt, ls, gg, dd):
+        rk.linear_logp_bwd_saved(hh, W, tt, ls, gg, saved, dh=dd, workspace=ws_bwd, stream=stream)
 
     def step(i):
-        rk.linear_logp(h, W, tg, out=logp, lse=lse, workspace=ws_fwd, stream=stream)
-        rk.linear_logp_bwd(h, W, tg, lse, g, dh=dh, workspace=ws_bwd, stream=stream)
+        fwd(h, tg, logp, lse)
+        bwd(h, tg, lse, g, dh)
         z, zt = zs[i % len(zs)]
         rk.logp_from_logits(z, zt, out=zlogp, lse=zlse, stream=stream)
 
@@ -499,9 +537,9 @@ def run_gpu(args) -> None:
         for i in range(args.steps):
             e = ev[i]
             e[0].record(stream)
-            rk.linear_logp(h, W, tg, out=logp, lse=lse, workspace=ws_fwd, stream=stream)
+            fwd(h, tg, logp, lse)
             e[1].record(stream)
-            rk.linear_logp_bwd(h, W, tg, lse, g, dh=dh, workspace=ws_bwd, stream=stream)
+            bwd(h, tg, lse, g, dh)
             e[2].record(stream)
             z, zt = zs[(args.warmup + i) % len(zs)]
             rk.logp_from_logits(z, zt, out=zlogp, lse=zlse, stream=stream)
@@ -580,10 +618,10 @@ def run_gpu(args) -> None:
         b["zt"].copy_(zth, non_blocking=True)
 
     def compute(b):
-        rk.linear_logp(b["h"], b["W"], b["tg"], out=b["logp"], lse=b["lse"], workspace=ws_fwd,
-                       stream=stream)
-        rk.linear_logp_bwd(b["h"], b["W"], b["tg"], b["lse"], b["g"], dh=b["dh"],
-                           workspace=ws_bwd, stream=stream)
+        rk.linear_logp_fwd_saved(b["h"], b["W"], b["tg"], out=b["logp"], lse=b["lse"],
+                                 saved=saved, stream=stream)
+        rk.linear_logp_bwd_saved(b["h"], b["W"], b["tg"], b["lse"], b["g"], saved, dh=b["dh"],
+                                 workspace=ws_bwd, stream=stream)
         rk.logp_from_logits(b["z"], b["zt"], out=b["zlogp"], lse=b["zlse"], stream=stream)
 
     def d2h_from(b):
@@ -639,15 +677,16 @@ def run_gpu(args) -> None:
             dist.destroy_process_group()
         return
 
-    flops_fwd = 2.0 * T * H * V
-    flops_bwd = 4.0 * T * H * V
+    flops_fwd = 2.0 * T * H * V   # z = h W^T with the fused softmax partials
+    flops_bwd = 2.0 * T * H * V   # dh = dZ W (dZ from the saved terms, no z recompute)
     tc_tflops = (flops_fwd + flops_bwd) / ((fwd_ms + bwd_ms) / 1000.0) / 1e12
     peak_tc = peaks["bf16_tflops_sustained"]
     lg_bytes = Tl * Vl * 2 + Tl * 8 + 2 * Tl * 4
     lg_gbs = lg_bytes / (lg_loop_ms / 1000.0) / 1e9
     lg_gbs_step = lg_bytes / (lg_ms / 1000.0) / 1e9
     traffic = None
-    if TRAFFIC_RECORD["source_sha1"] == kernel_source_sha1() and (T, H, V) == (65536, 4096, 128256):
+    if (TRAFFIC_RECORD["source_sha1"] == kernel_source_sha1()
+            and (T, H, V) == (65536, 4096, 128256)):
         traffic = TRAFFIC_RECORD["bytes_per_step"]
 
     rows = None
@@ -670,14 +709,15 @@ def run_gpu(args) -> None:
                          f"{N_LOGITS_BUFFERS} buffers of {Tl * Vl * 2 / 1e6:.0f} MB"},
         "roofline": {"bound": "tensor", "achieved": tc_tflops, "peak": peak_tc,
                      "unit": "TFLOP/s", "frac": tc_tflops / peak_tc, "traffic": traffic,
-                     "kernel": "linear_logp_tiles (fwd + dZ + dh launches; each timed with the "
-                               "small kernels of its call)",
-                     "algorithmic": "6*T*H*V flop per step (2 fwd + 2 z-recompute + 2 dZ.W)",
-                     "traffic_unit": "DRAM bytes per step (3 tile launches, ncu)",
+                     "kernel": "linear_logp_tiles (the forward launch and the dh GEMM launch, "
+                               "each timed with the rest of its call: the backward call also "
+                               "holds the HBM-bound pass that turns the saved terms into dZ)",
+                     "algorithmic": "4*T*H*V flop per step (2 fwd + 2 dZ.W)",
+                     "traffic_unit": "DRAM bytes per step (2 tile launches, ncu)",
                      "traffic_per_launch_gb": TRAFFIC_RECORD["per_launch_gb"] if traffic else None,
                      "algorithmic_bytes": algorithmic_bytes_per_step(T, H, V),
                      "peak_source": f"{peaks['source']} bf16_tflops_sustained"},
-        "components_ms": {"linear_logp_fwd": fwd_ms, "linear_logp_bwd": bwd_ms,
+        "components_ms": {"linear_logp_fwd_saved": fwd_ms, "linear_logp_bwd_saved": bwd_ms,
                           "logits_path": lg_ms},
         "fwd_tflops": flops_fwd / (fwd_ms / 1000.0) / 1e12,
         "bwd_tflops": flops_bwd / (bwd_ms / 1000.0) / 1e12,
@@ -754,6 +794,17 @@ def run_case(args) -> None:
             dW = torch.empty((V, H), dtype=torch.float32, device=dev)
             fn = lambda: rk.linear_logp_dw(h, W, tg, lse, g, dW=dW, workspace=ws)
             flops = 4.0 * T * H * V
+        elif args.case == "saved":
+            # forward that keeps its softmax terms + the backward from them
+            saved = torch.empty(rk.linear_logp_saved_size(T, H, V), dtype=torch.uint8, device=dev)
+            wsb = torch.empty(rk.linear_logp_bwd_saved_workspace_size(T, H, V), dtype=torch.uint8,
+                              device=dev)
+            dh = torch.empty((T, H), dtype=torch.float32, device=dev)
+
+            def fn():
+                _, lse_s, _ = rk.linear_logp_fwd_saved(h, W, tg, saved=saved)
+                rk.linear_logp_bwd_saved(h, W, tg, lse_s, g, saved, dh=dh, workspace=wsb)
+            flops = 4.0 * T * H * V
         elif args.case == "full":
             ws = torch.empty(rk.linear_logp_bwd_full_workspace_size(T, H, V), dtype=torch.uint8,
                              device=dev)
@@ -793,7 +844,7 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the separate timing of the widened rows")
-    ap.add_argument("--case", choices=["fwd", "bwd", "logits", "logits_bwd", "dw", "full"],
+    ap.add_argument("--case", choices=["fwd", "bwd", "logits", "logits_bwd", "dw", "full", "saved"],
                     default=None)
     ap.add_argument("--shape", default="2048,4096,32000")
     ap.add_argument("--reps", type=int, default=3)

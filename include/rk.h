@@ -167,6 +167,52 @@ rk_status rk_linear_logp_bwd(const uint16_t *h, const uint16_t *W, const int64_t
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The same forward and backward with the softmax terms kept between them, so
+ * that the backward need not recompute z = h W^T with a second GEMM (HBM is
+ * large enough to hold them: 16.8 GB for T = 65536, V = 128256).
+ *
+ * rk_linear_logp_fwd_saved is rk_linear_logp that also writes, into `saved`,
+ * every row's per-tile softmax terms e[t, v] = exp(z[t, v] - m), in bf16, with
+ * m the row's maximum over the 256-column vocabulary tile holding v, next to
+ * the tiles' (max, sum) partials.  Its logp and lse are bitwise those of
+ * rk_linear_logp.
+ *
+ * rk_linear_logp_bwd_saved computes dh as rk_linear_logp_bwd defines it
+ * (issue #244, Workstream 3 #153: fixed, batch-shape-independent order, no
+ * atomicAdd), from `saved` instead of a z recompute:
+ *   p[t, v]  = exp(m - lse[t]) * e[t, v],   dZ = g p rounded to bf16,
+ *   dh[t, :] = sum over the row's fp32 entries of w W[v, :] - dZ[t, :] W
+ * where the entries are the target column and the columns with p >= 1/64,
+ * whose w = g (onehot - p) uses an exact fp32 z = h[t] . W[v] (one fixed
+ * order).  dZ carries two bf16 roundings (of e, then of g p) where the
+ * recompute path carries one; the fp32 entries keep peaked softmaxes exact.
+ * The bits differ from rk_linear_logp_bwd's; they are again a function of
+ * the row alone (bitwise batch-invariant) and within the same tolerance.
+ * The call turns the terms in `saved` into dZ in place, so a saved state
+ * serves one backward.
+ *
+ *   saved      >= rk_linear_logp_saved_size(T, H, V) bytes, 256-byte aligned
+ *              (caller-owned; written by the forward, consumed by the backward)
+ *   workspace  >= rk_linear_logp_bwd_saved_workspace_size(T, H, V) bytes
+ *              (tile counter, the rows' entry counts and lists), 16-byte aligned
+ *   h, W, targets, cu_seqlens, lse, grad_logp, dh: as for rk_linear_logp_bwd
+ *              (same h, W, targets, cu_seqlens as the forward that filled `saved`)
+ * Supported: as rk_linear_logp, and V < 65535 * 8192.
+ */
+size_t rk_linear_logp_saved_size(int64_t T, int64_t H, int64_t V);
+rk_status rk_linear_logp_fwd_saved(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                                   const int32_t *cu_seqlens, int32_t num_seqs,
+                                   int64_t T, int64_t H, int64_t V, float *logp, float *lse,
+                                   void *saved, size_t saved_bytes, void *stream);
+size_t rk_linear_logp_bwd_saved_workspace_size(int64_t T, int64_t H, int64_t V);
+rk_status rk_linear_logp_bwd_saved(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                                   const int32_t *cu_seqlens, int32_t num_seqs,
+                                   int64_t T, int64_t H, int64_t V,
+                                   const float *lse, const float *grad_logp,
+                                   void *saved, size_t saved_bytes, float *dh,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * The dense path's lm_head (chain index 6 of PR #264; "dense vs indexed
  * selected-logprob paths", issue #101, Scope): logits[t, v] = bf16(sum_k
  * h[t, k] * W[v, k]) with fp32 accumulation and one rounding to bf16, using the

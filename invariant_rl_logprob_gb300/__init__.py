@@ -28,6 +28,8 @@ __all__ = [
     "logp_from_logits",
     "linear_logp_bwd", "linear_logp_bwd_workspace_size", "linear_logp_bwd_min_workspace_size",
     "lm_head", "logp_from_logits_bwd", "grpo_token_loss", "linear_logp_grpo", "linear_greedy",
+    "linear_logp_fwd_saved", "linear_logp_bwd_saved", "linear_logp_saved_size",
+    "linear_logp_bwd_saved_workspace_size",
     "linear_greedy_workspace_size", "linear_logp_dw", "linear_logp_dw_workspace_size",
     "linear_logp_bwd_full", "linear_logp_bwd_full_workspace_size", "lm_head_workspace_size",
     "get_device_error", "selftest_wait_timeout", "set_row_blocks", "last_row_blocks", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT", "DEVERR_LSE",
@@ -119,6 +121,15 @@ def load_library() -> ctypes.CDLL:
     lib.rk_linear_logp_grpo.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, f32, f32,
                                         f32, f32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.rk_linear_logp_grpo.restype = ctypes.c_int
+    lib.rk_linear_logp_saved_size.argtypes = [i64, i64, i64]
+    lib.rk_linear_logp_saved_size.restype = sz
+    lib.rk_linear_logp_fwd_saved.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, sz, vp]
+    lib.rk_linear_logp_fwd_saved.restype = ctypes.c_int
+    lib.rk_linear_logp_bwd_saved_workspace_size.argtypes = [i64, i64, i64]
+    lib.rk_linear_logp_bwd_saved_workspace_size.restype = sz
+    lib.rk_linear_logp_bwd_saved.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, sz, vp,
+                                             vp, sz, vp]
+    lib.rk_linear_logp_bwd_saved.restype = ctypes.c_int
     lib.rk_set_row_blocks.argtypes = [i32]
     lib.rk_set_row_blocks.restype = ctypes.c_int
     lib.rk_last_row_blocks.argtypes = [i32]
@@ -365,6 +376,71 @@ def linear_logp_grpo(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor,
                                  _stream_handle(stream, h.device))
     _check(st, "rk_linear_logp_grpo")
     return out
+
+
+def linear_logp_saved_size(T: int, H: int, V: int) -> int:
+    return int(load_library().rk_linear_logp_saved_size(T, H, V))
+
+
+def linear_logp_bwd_saved_workspace_size(T: int, H: int, V: int) -> int:
+    return int(load_library().rk_linear_logp_bwd_saved_workspace_size(T, H, V))
+
+
+def linear_logp_fwd_saved(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor,
+                          cu_seqlens: torch.Tensor | None = None, *,
+                          out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                          saved: torch.Tensor | None = None,
+                          stream: torch.cuda.Stream | None = None):
+    """linear_logp that also keeps its softmax terms for
+    :func:`linear_logp_bwd_saved`: returns ``(logp, lse, saved)``."""
+    lib = load_library()
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    T, H = h.shape
+    V = W.shape[0]
+    if W.shape[1] != H or W.device != h.device:
+        raise ValueError("W must be [V, H] on h's device")
+    cu, ns = _rows(targets, cu_seqlens, T, h.device)
+    if out is None:
+        out = torch.empty(T, dtype=torch.float32, device=h.device)
+    if lse is None:
+        lse = torch.empty(T, dtype=torch.float32, device=h.device)
+    if saved is None:
+        saved = torch.empty(max(int(lib.rk_linear_logp_saved_size(T, H, V)), 1), dtype=torch.uint8,
+                            device=h.device)
+    st = lib.rk_linear_logp_fwd_saved(_ptr(h), _ptr(W), _ptr(targets), _ptr(cu), ns, T, H, V,
+                                      _ptr(out), _ptr(lse), _ptr(saved), saved.numel(),
+                                      _stream_handle(stream, h.device))
+    _check(st, "rk_linear_logp_fwd_saved")
+    return out, lse, saved
+
+
+def linear_logp_bwd_saved(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor,
+                          lse: torch.Tensor, grad_logp: torch.Tensor, saved: torch.Tensor,
+                          cu_seqlens: torch.Tensor | None = None, *,
+                          dh: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                          stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """dh fp32 ``[T, H]`` from the state :func:`linear_logp_fwd_saved` kept
+    (which this call consumes)."""
+    lib = load_library()
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    _need(lse, "lse", torch.float32, 1)
+    _need(grad_logp, "grad_logp", torch.float32, 1)
+    T, H = h.shape
+    V = W.shape[0]
+    cu, ns = _rows(targets, cu_seqlens, T, h.device)
+    if dh is None:
+        dh = torch.empty((T, H), dtype=torch.float32, device=h.device)
+    if workspace is None:
+        need = int(lib.rk_linear_logp_bwd_saved_workspace_size(T, H, V))
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
+    st = lib.rk_linear_logp_bwd_saved(_ptr(h), _ptr(W), _ptr(targets), _ptr(cu), ns, T, H, V,
+                                      _ptr(lse), _ptr(grad_logp), _ptr(saved), saved.numel(),
+                                      _ptr(dh), _ptr(workspace), workspace.numel(),
+                                      _stream_handle(stream, h.device))
+    _check(st, "rk_linear_logp_bwd_saved")
+    return dh
 
 
 def linear_greedy_workspace_size(T: int, H: int, V: int) -> int:

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "librk.so")
-SOURCES = ["rk_api.cu", "logits_logp.cu", "linear_logp_tc.cu", "rk_noalloc.cu", "token_loss.cu", "dw_prep.cu"]
+SOURCES = ["rk_api.cu", "logits_logp.cu", "linear_logp_tc.cu", "rk_noalloc.cu", "token_loss.cu",
+           "dw_prep.cu", "saved_bwd.cu"]
 HEADERS = ["rk_device.cuh", "rk_internal.h", "token_loss.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -92,8 +92,13 @@ constexpr int kGroupNDh = 8;  // raster group (in H tiles) of the dh and dW GEMM
 // one-hot term added in the epilogue.
 // kDh2, kDwK2: kDh and kDwK with two row blocks per tile (see TileCfg).
 enum Mode {
-    kFwd = 0, kDz = 1, kDh = 2, kLogits = 3, kGreedy = 4, kDzT = 6, kDwK = 7, kDh2 = 8, kDwK2 = 9
+    kFwd = 0, kDz = 1, kDh = 2, kLogits = 3, kGreedy = 4, kDzT = 6, kDwK = 7, kDh2 = 8, kDwK2 = 9,
+    kFwdS = 10
 };
+// kFwdS: kFwd that also saves, for the backward, every row's
+// e = 2^((z - m_tile) log2 e) in bf16 (the terms of the tile's sum-exp, m_tile
+// the row's maximum over the tile) through TMA stores.
+__host__ __device__ constexpr bool mode_fwd(int m) { return m == kFwd || m == kFwdS; }
 __host__ __device__ constexpr bool mode_dh(int m) { return m == kDh || m == kDh2; }
 __host__ __device__ constexpr bool mode_dw(int m) { return m == kDwK || m == kDwK2; }
 
@@ -140,7 +145,7 @@ struct TileCfg {
     static constexpr int kStgBytes = kMB * kABytes + kBBytes;
     static constexpr size_t kSmem =
         1024 + (size_t)kStg * kStgBytes + kCtlBytes +
-        ((MODE == 1 /* kDz */ || MODE == 6 /* kDzT */) ? kStageTBytes : 0);
+        ((MODE == 1 /* kDz */ || MODE == 6 /* kDzT */ || MODE == 10 /* kFwdS */) ? kStageTBytes : 0);
     static_assert(kStg <= kStages, "stage barriers");
     static_assert(kSmem <= 227 * 1024, "shared memory");
 };
@@ -490,12 +495,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const bool in_range = lrow < a.rows;
             const int64_t grow = a.row0 + lrow;                    // global row
             // the row's target (forward and dZ tiles only: kDzT rows are vocabulary rows)
-            const int64_t tgt = ((MODE == kFwd || MODE == kDz) && in_range && a.targets != nullptr)
+            const int64_t tgt = ((mode_fwd(MODE) || MODE == kDz) && in_range && a.targets != nullptr)
                                     ? a.targets[grow]
                                     : -1;
             const int n0 = nb * BN;
             const uint32_t empty_bar = mapa_shared(smem_u32(&ctl->tmem_empty[b]), 0);
-            if constexpr (MODE == kFwd || MODE == kGreedy) {
+            if constexpr (mode_fwd(MODE) || MODE == kGreedy) {
                 const int valid = min(BN, a.V - n0);
                 const int tcol = (tgt >= n0 && tgt < (int64_t)n0 + valid) ? (int)(tgt - n0) : -1;
                 if (!warp_wait(smem_u32(&ctl->tmem_full[b]), tph, abort, a.err)) break;
@@ -555,6 +560,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         acc1 = __fadd_rn(acc1, e[j + 1]);
                         acc2 = __fadd_rn(acc2, e[j + 2]);
                         acc3 = __fadd_rn(acc3, e[j + 3]);
+                    }
+                    if constexpr (MODE == kFwdS) {
+                        // the warp's 32 x 32 block of e, in bf16, through one TMA
+                        // store (clipped at V and at the rows), staged as in kDz
+                        uint16_t *sbz = stageT + (warp * 4 + (int)(tchunks & 1) * 2) * kStageT;
+                        if (lane == 0 && tchunks >= 2) bulk_wait_group_read<1>();
+                        __syncwarp();
+                        uint8_t *rowp = reinterpret_cast<uint8_t *>(sbz) + lane * 64;
+                        const int sw = (lane >> 1) & 3;
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq)
+                            *reinterpret_cast<uint4 *>(rowp + ((qq ^ sw) << 4)) = make_uint4(
+                                pack_bf16x2(e[8 * qq], e[8 * qq + 1]), pack_bf16x2(e[8 * qq + 2], e[8 * qq + 3]),
+                                pack_bf16x2(e[8 * qq + 4], e[8 * qq + 5]), pack_bf16x2(e[8 * qq + 6], e[8 * qq + 7]));
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int64_t r0 = (int64_t)mb * 2 * BM + (int64_t)rank * BM + warp * 32;
+                            tma_store_2d(&tmD, smem_u32(sbz), n0 + c * 32, (int32_t)r0);
+                            bulk_commit_group();
+                        }
+                        ++tchunks;
                     }
                     const int rel = tcol - c * 32;
                     if (rel >= 0 && rel < 32) {
@@ -899,9 +926,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     }
 
-    if constexpr (MODE == kDz || MODE == kDzT) {
+    if constexpr (MODE == kDz || MODE == kDzT || MODE == kFwdS) {
         // staged blocks must be read out of shared memory and written
-        if (warp < kEpiThreads / 32 && lane == 0 && (a.dzT_store || a.dz_tma)) bulk_wait_group_all();
+        if (warp < kEpiThreads / 32 && lane == 0 && (a.dzT_store || a.dz_tma || MODE == kFwdS))
+            bulk_wait_group_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -1171,6 +1199,117 @@ cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_
     else
         linear_logp_merge<false><<<mgrid, 32 * kMergeRowsPerBlock, 0, st>>>(
             a.part, a.ztgt, targets, cu, num_seqs, T, a.V, a.num_n, logp, lse, di.err, GrpoArgs{});
+    return cudaGetLastError();
+}
+
+// ---- forward that saves its exponentials, and the backward that uses them ----
+// Saved state: the forward workspace (tile partials, target logits, tile
+// counter), then e = bf16(2^((z - m_tile) log2 e)) as [T][ld_dz(V)].
+size_t linear_fwd_saved_bytes(int64_t T, int64_t V) {
+    if (T <= 0) return 0;
+    return linear_fwd_workspace_bytes(T, V) + round256((size_t)T * (size_t)ld_dz(V) * 2);
+}
+
+cudaError_t launch_linear_fwd_saved(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                                    const int32_t *cu, int num_seqs, int64_t T, int64_t H,
+                                    int64_t V, float *logp, float *lse, void *saved,
+                                    const DeviceInfo &di, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    CUtensorMap tmA, tmB, tmS;
+    if (!encode_tmap_bf16_2d(&tmA, h, (uint64_t)H, (uint64_t)T, (uint64_t)H * 2, BK, BM, true))
+        return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16_2d(&tmB, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2, true))
+        return cudaErrorInvalidValue;
+    uint8_t *w = reinterpret_cast<uint8_t *>(saved);
+    const size_t fwd_bytes = linear_fwd_workspace_bytes(T, V);
+    uint16_t *stash = reinterpret_cast<uint16_t *>(w + fwd_bytes);
+    if (!encode_tmap_bf16_2d_sw64(&tmS, stash, (uint64_t)V, (uint64_t)T, (uint64_t)ld_dz(V) * 2, 32,
+                                  32))
+        return cudaErrorInvalidValue;
+    TileArgs a{};
+    a.targets = targets;
+    a.cu = cu;
+    a.num_seqs = num_seqs;
+    a.row0 = 0;
+    a.rows = T;
+    a.V = (int32_t)V;
+    a.H = (int32_t)H;
+    a.num_m = (int32_t)((T + 2 * BM - 1) / (2 * BM));
+    a.num_n = (int32_t)((V + BN - 1) / BN);
+    a.num_k = (int32_t)(H / BK);
+    a.err = di.err;
+    a.part = reinterpret_cast<float2 *>(w);
+    a.ztgt = reinterpret_cast<float *>(w + round256((size_t)T * (size_t)a.num_n * sizeof(float2)));
+    a.tile_counter = reinterpret_cast<unsigned *>(w + fwd_bytes - kCounterBytes);
+    cudaError_t e = run_tiles<kFwdS>(tmA, tmB, a, di, st, nullptr, &tmS);
+    if (e != cudaSuccess) return e;
+    const unsigned mgrid = (unsigned)((T + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock);
+    linear_logp_merge<false><<<mgrid, 32 * kMergeRowsPerBlock, 0, st>>>(
+        a.part, a.ztgt, targets, cu, num_seqs, T, a.V, a.num_n, logp, lse, di.err, GrpoArgs{});
+    return cudaGetLastError();
+}
+
+size_t linear_bwd_saved_workspace_bytes(int64_t T) {
+    if (T <= 0) return 0;
+    const size_t r = (size_t)T;
+    return kCounterBytes + round256(r * 4) + round256(r * (size_t)kEntCap * 8);
+}
+
+cudaError_t launch_linear_bwd_saved(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                                    const int32_t *cu, int num_seqs, int64_t T, int64_t H,
+                                    int64_t V, const float *lse, const float *grad, void *saved,
+                                    float *dh, void *workspace, const DeviceInfo &di,
+                                    cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const int64_t ldz = ld_dz(V);
+    const int32_t num_n = (int32_t)((V + BN - 1) / BN);
+    uint8_t *sv = reinterpret_cast<uint8_t *>(saved);
+    const float2 *part = reinterpret_cast<const float2 *>(sv);
+    uint16_t *dz = reinterpret_cast<uint16_t *>(sv + linear_fwd_workspace_bytes(T, V));
+    uint8_t *w = reinterpret_cast<uint8_t *>(workspace);
+    unsigned *counter = reinterpret_cast<unsigned *>(w);
+    int32_t *ecount = reinterpret_cast<int32_t *>(w + kCounterBytes);
+    int2 *ent = reinterpret_cast<int2 *>(w + kCounterBytes + round256((size_t)T * 4));
+
+    // the saved exponentials become dZ in place; the target and p >= 1/64
+    // columns become the rows' fp32 entries, weighted from an exact z
+    cudaError_t e = cudaMemsetAsync(ecount, 0, (size_t)T * 4, st);
+    if (e != cudaSuccess) return e;
+    e = launch_stash_to_dz(dz, ldz, part, num_n, targets, cu, num_seqs, T, V, lse, grad, ecount,
+                           ent, di, st);
+    if (e != cudaSuccess) return e;
+    e = launch_exact_entries(h, W, H, targets, cu, num_seqs, T, V, lse, grad, ecount, ent, st);
+    if (e != cudaSuccess) return e;
+    e = launch_sort_entries(ecount, ent, T, st);
+    if (e != cudaSuccess) return e;
+
+    // dh = (the row's fp32 entries) . W - dZ W, K = V in one ascending pass
+    CUtensorMap tmDz, tmW_mn;
+    if (!encode_tmap_bf16_2d(&tmDz, dz, (uint64_t)V, (uint64_t)T, (uint64_t)ldz * 2, BK, BM, true))
+        return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16_2d(&tmW_mn, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, 64, BK, true))
+        return cudaErrorInvalidValue;
+    TileArgs a{};
+    a.tile_counter = counter;
+    a.targets = targets;
+    a.cu = cu;
+    a.num_seqs = num_seqs;
+    a.row0 = 0;
+    a.rows = T;
+    a.V = (int32_t)V;
+    a.H = (int32_t)H;
+    a.err = di.err;
+    a.W = W;
+    a.dh = dh;
+    a.ecount = ecount;
+    a.ent = ent;
+    a.num_m = (int32_t)((T + 2 * BM - 1) / (2 * BM));
+    a.num_n = (int32_t)((H + BN - 1) / BN);
+    a.num_k = (int32_t)((V + BK - 1) / BK);
+    e = run_rows<kDh, kDh2>(tmDz, tmW_mn, a, di, st, RowGemm::kDhGemm);
+    if (e != cudaSuccess) return e;
+    linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(targets, cu, num_seqs, T, (int32_t)V,
+                                                          (int32_t)H, dh, di.err);
     return cudaGetLastError();
 }
 

@@ -207,6 +207,70 @@ rk_status rk_linear_logp_grpo(const uint16_t *h, const uint16_t *W, const int64_
     return RK_OK;
 }
 
+size_t rk_linear_logp_saved_size(int64_t T, int64_t H, int64_t V) {
+    (void)H;
+    if (T <= 0 || V <= 0) return 0;
+    return rk::linear_fwd_saved_bytes(T, V);
+}
+
+rk_status rk_linear_logp_fwd_saved(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                                   const int32_t *cu_seqlens, int32_t num_seqs, int64_t T,
+                                   int64_t H, int64_t V, float *logp, float *lse, void *saved,
+                                   size_t saved_bytes, void *stream) {
+    if (T < 0 || H <= 0 || V <= 0) return RK_ERR_INVALID_ARG;
+    if (T == 0) return RK_OK;
+    if (!h || !W || !logp) return RK_ERR_INVALID_ARG;
+    rk_status st = check_rows(targets, cu_seqlens, num_seqs);
+    if (st != RK_OK) return st;
+    if (H % 64 != 0 || H > 65536 || V >= (int64_t(1) << 31) || T >= (int64_t(1) << 31))
+        return RK_ERR_UNSUPPORTED;
+    if (!aligned(h, 16) || !aligned(W, 16)) return RK_ERR_UNSUPPORTED;
+    if (!saved || saved_bytes < rk::linear_fwd_saved_bytes(T, V)) return RK_ERR_WORKSPACE;
+    if (!aligned(saved, 256)) return RK_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    e = rk::launch_linear_fwd_saved(h, W, targets, cu_seqlens, num_seqs, T, H, V, logp, lse, saved,
+                                    di, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    return RK_OK;
+}
+
+size_t rk_linear_logp_bwd_saved_workspace_size(int64_t T, int64_t H, int64_t V) {
+    (void)H;
+    if (T <= 0 || V <= 0) return 0;
+    return rk::linear_bwd_saved_workspace_bytes(T);
+}
+
+rk_status rk_linear_logp_bwd_saved(const uint16_t *h, const uint16_t *W, const int64_t *targets,
+                                   const int32_t *cu_seqlens, int32_t num_seqs, int64_t T,
+                                   int64_t H, int64_t V, const float *lse,
+                                   const float *grad_logp, void *saved, size_t saved_bytes,
+                                   float *dh, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
+    if (T < 0 || H <= 0 || V <= 0) return RK_ERR_INVALID_ARG;
+    if (T == 0) return RK_OK;
+    if (!h || !W || !lse || !grad_logp || !dh) return RK_ERR_INVALID_ARG;
+    rk_status st = check_rows(targets, cu_seqlens, num_seqs);
+    if (st != RK_OK) return st;
+    if (H % 64 != 0 || H > 65536 || V >= (int64_t(1) << 31) || T >= (int64_t(1) << 31))
+        return RK_ERR_UNSUPPORTED;
+    if ((V + 8191) / 8192 > 65535) return RK_ERR_UNSUPPORTED;
+    if (!aligned(h, 16) || !aligned(W, 16) || !aligned(dh, 16)) return RK_ERR_UNSUPPORTED;
+    if (!saved || saved_bytes < rk::linear_fwd_saved_bytes(T, V)) return RK_ERR_WORKSPACE;
+    if (!aligned(saved, 256)) return RK_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < rk::linear_bwd_saved_workspace_bytes(T))
+        return RK_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return RK_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    e = rk::launch_linear_bwd_saved(h, W, targets, cu_seqlens, num_seqs, T, H, V, lse, grad_logp,
+                                    saved, dh, workspace, di, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    return RK_OK;
+}
+
 rk_status rk_logp_from_logits(const uint16_t *logits, const int64_t *targets,
                               const int32_t *cu_seqlens, int32_t num_seqs, int64_t T, int64_t V,
                               float *logp, float *lse, void *stream) {

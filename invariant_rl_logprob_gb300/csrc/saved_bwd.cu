@@ -1,0 +1,159 @@
+// saved_bwd.cu -- the two elementwise steps of the linear_logp backward that
+// starts from the forward's saved state instead of recomputing z = h W^T
+// (issue #244 "[WS1 Test] ...", Workstream 3 #153: fixed,
+// batch-shape-independent order, no atomicAdd on values).
+//
+// The forward (tile mode kFwdS) saved, per row t and vocabulary tile j of 256
+// columns, the tile maximum m_tj and e[t, v] = bf16(2^((z - m_tj) log2 e)).
+// With lse from the forward and the upstream gradient g,
+//   p[t, v] = e^(m_tj - lse_t) * e[t, v]
+// is the row's softmax up to the bf16 rounding of e, and
+//   stash_to_dz   rewrites e in place into dZ = bf16(g e^(m_tj - lse) e) on
+//                 every column except the target and the columns with
+//                 p >= 1/64, which it leaves as 0 and lists as the row's fp32
+//                 entries (as the recompute path does);
+//   exact_entries gives each listed column its fp32 weight
+//                 w = g (onehot - p) from an exact z = h_t . W_v (fp32, one
+//                 fixed order), so a peaked softmax never puts a rounded large
+//                 term into dh.
+// Each element and each entry depends only on its row, so a row's results do
+// not depend on the batch around it.
+#include "rk_device.cuh"
+#include "rk_internal.h"
+
+namespace rk {
+namespace {
+
+constexpr int kConvThreads = 256;
+constexpr int kConvGroupsPerThread = 4;
+constexpr int64_t kConvCols = (int64_t)kConvThreads * 8 * kConvGroupsPerThread;  // 8192 per block
+constexpr int kTileCols = 256;  // the forward's vocabulary tile
+
+__device__ __noinline__ void list_entry(int64_t col, int32_t *count, int2 *list, unsigned *err) {
+    const int slot = atomicAdd(count, 1);
+    if (slot < kEntCap)
+        list[slot] = make_int2((int)col, 0);
+    else
+        atomicOr(err, kErrLse);
+}
+
+// grid (T, ceil(V / kConvCols)): block (t, q) takes columns
+// [q kConvCols, (q + 1) kConvCols) of row t, 8 consecutive columns per thread
+// and group (a group of 8 never crosses a 256-column tile).
+__global__ void __launch_bounds__(kConvThreads)
+    stash_to_dz(uint16_t *__restrict__ dz, int64_t ldz, const float2 *__restrict__ part,
+                int32_t num_n, const int64_t *__restrict__ targets, const int32_t *__restrict__ cu,
+                int num_seqs, int64_t V, const float *__restrict__ lse,
+                const float *__restrict__ grad, int32_t *__restrict__ ecount,
+                int2 *__restrict__ ent, unsigned *err) {
+    const int64_t row = blockIdx.x;
+    const int64_t tgt = targets[row];
+    const bool active = row_active(row, tgt, cu, num_seqs) && tgt < V;
+    uint16_t *drow = dz + row * ldz;
+    const float g = active ? grad[row] : 0.f;
+    const float l = active ? lse[row] : 0.f;
+#pragma unroll
+    for (int i = 0; i < kConvGroupsPerThread; ++i) {
+        const int64_t c0 = (int64_t)blockIdx.y * kConvCols + (int64_t)i * (kConvThreads * 8) +
+                           (int64_t)threadIdx.x * 8;
+        if (c0 >= V) continue;
+        uint4 *gp = reinterpret_cast<uint4 *>(drow + c0);  // ldz % 8 == 0: 16-byte aligned
+        if (!active) {
+            *gp = make_uint4(0, 0, 0, 0);
+            continue;
+        }
+        const float mt = part[row * num_n + c0 / kTileCols].x;
+        const float f = ex2(__fmul_rn(__fsub_rn(mt, l), kLog2e));  // e^(m_tj - lse) <= 1
+        const float c = __fmul_rn(g, f);
+        const uint4 w = *gp;
+        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float d[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int64_t col = c0 + 2 * k + hh;
+                const float e = hh ? bf16_hi(q[k]) : bf16_lo(q[k]);
+                d[hh] = 0.f;
+                if (col < V) {
+                    if (col == tgt || __fmul_rn(f, e) >= kEntTau)
+                        list_entry(col, ecount + row, ent + row * kEntCap, err);
+                    else
+                        d[hh] = __fmul_rn(c, e);
+                }
+            }
+            o[k] = pack_bf16x2(d[0], d[1]);
+        }
+        *gp = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// One warp per row: each listed column's exact z = h_t . W_v, summed in fp32
+// with lane l taking the 8-element groups l, l + 32, ... (products exact in
+// fp32, added in group order), then a fixed xor tree; w = g (onehot - p).
+constexpr int kExactRowsPerBlock = 8;
+__global__ void __launch_bounds__(32 * kExactRowsPerBlock)
+    exact_entries(const uint16_t *__restrict__ h, const uint16_t *__restrict__ W, int64_t H,
+                  const int64_t *__restrict__ targets, const int32_t *__restrict__ cu,
+                  int num_seqs, int64_t T, int64_t V, const float *__restrict__ lse,
+                  const float *__restrict__ grad, const int32_t *__restrict__ ecount,
+                  int2 *__restrict__ ent) {
+    const int64_t row = (int64_t)blockIdx.x * kExactRowsPerBlock + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= T) return;
+    const int64_t tgt = targets[row];
+    if (!row_active(row, tgt, cu, num_seqs) || tgt >= V) return;
+    const int n = min(ecount[row], kEntCap);
+    const float g = grad[row];
+    const float l = lse[row];
+    const uint4 *hr = reinterpret_cast<const uint4 *>(h + row * H);
+    int2 *el = ent + row * kEntCap;
+    for (int e = 0; e < n; ++e) {
+        const int v = el[e].x;
+        const uint4 *wr = reinterpret_cast<const uint4 *>(W + (int64_t)v * H);
+        float acc = 0.f;
+        for (int64_t k8 = lane; k8 < H / 8; k8 += 32) {
+            const uint4 a = __ldg(hr + k8), b = __ldg(wr + k8);
+            const uint32_t qa[4] = {a.x, a.y, a.z, a.w}, qb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc = __fmaf_rn(bf16_lo(qa[j]), bf16_lo(qb[j]), acc);
+                acc = __fmaf_rn(bf16_hi(qa[j]), bf16_hi(qb[j]), acc);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+        const float p = ex2(__fmul_rn(__fsub_rn(acc, l), kLog2e));
+        const float w = __fmul_rn(g, __fsub_rn(v == tgt ? 1.f : 0.f, p));
+        if (lane == 0) el[e].y = __float_as_int(w);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_stash_to_dz(uint16_t *dz, int64_t ldz, const float2 *part, int32_t num_n,
+                               const int64_t *targets, const int32_t *cu, int num_seqs, int64_t T,
+                               int64_t V, const float *lse, const float *grad, int32_t *ecount,
+                               int2 *ent, const DeviceInfo &di, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const int64_t segs = (V + kConvCols - 1) / kConvCols;
+    if (segs > 65535) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)T, (unsigned)segs);
+    stash_to_dz<<<grid, kConvThreads, 0, st>>>(dz, ldz, part, num_n, targets, cu, num_seqs, V, lse,
+                                              grad, ecount, ent, di.err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_exact_entries(const uint16_t *h, const uint16_t *W, int64_t H,
+                                 const int64_t *targets, const int32_t *cu, int num_seqs, int64_t T,
+                                 int64_t V, const float *lse, const float *grad,
+                                 const int32_t *ecount, int2 *ent, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)((T + kExactRowsPerBlock - 1) / kExactRowsPerBlock);
+    exact_entries<<<grid, 32 * kExactRowsPerBlock, 0, st>>>(h, W, H, targets, cu, num_seqs, T, V,
+                                                           lse, grad, ecount, ent);
+    return cudaGetLastError();
+}
+
+}  // namespace rk

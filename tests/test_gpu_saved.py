@@ -1,0 +1,150 @@
+"""The forward that keeps its softmax terms and the backward that uses them
+(rk_linear_logp_fwd_saved / rk_linear_logp_bwd_saved): the forward's logp and
+lse are bitwise rk_linear_logp's; dh matches the fp64 oracle (relation A) on
+every shape, mask and peaked regime the recompute path is checked on; and dh
+is bitwise invariant under the batch transforms (relation I; PR #264
+"docs(ws1): batch-invariance contract RFC", T1-T6)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_rl_logprob_gb300 import contract, synth
+from tests.helpers import DEV, bits_np, cuda, oracle_bwd, same_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rk():
+    from invariant_rl_logprob_gb300 import build
+    build.build()
+    import invariant_rl_logprob_gb300 as m
+    m.load_library()
+    m.get_device_error()
+    return m
+
+
+def _saved_fwd_bwd(rk, h, W, tg, g, cu=None):
+    logp, lse, saved = rk.linear_logp_fwd_saved(h, W, tg, cu)
+    dh = rk.linear_logp_bwd_saved(h, W, tg, lse, g, saved, cu)
+    return logp, lse, dh
+
+
+@pytest.mark.parametrize("T,H,V", [(300, 64, 1000), (129, 192, 4097), (1, 128, 5), (257, 256, 769),
+                                   (700, 128, 2001), (64, 256, 4096), (513, 512, 20000)])
+def test_saved_path_vs_oracle(rk, T, H, V):
+    gen = synth.generator(8000 + T + H + V)
+    W = synth.normal_bf16(gen, (V, H), 0.05)
+    h = synth.normal_bf16(gen, (T, H), 1.0)
+    tg = synth.uniform_targets(gen, T, V)
+    tg[::13] = -100
+    g = torch.randn(T, generator=gen, dtype=torch.float32)
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    logp, lse, dh = _saved_fwd_bwd(rk, hd, Wd, tgd, gd)
+    lp0, lse0 = rk.linear_logp(hd, Wd, tgd)
+    assert same_bits(logp, lp0) and same_bits(lse, lse0)
+    ref = oracle_bwd(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy())
+    chk = contract.check_gradient_accuracy(dh.cpu().numpy(), ref)
+    assert chk.passed, chk
+    assert torch.all(dh.cpu()[::13] == 0)
+    assert rk.get_device_error() == 0
+
+
+@pytest.mark.parametrize("w_std,argmax_targets", [(0.25, True), (0.4, True), (0.4, False)])
+def test_saved_path_peaked_softmax(rk, w_std, argmax_targets):
+    # logit std ~6-9: the target (or another column) holds most of the mass;
+    # those columns come from an exact z, so dh stays inside the tolerance
+    T, H, V = 512, 512, 4096
+    gen = synth.generator(123)
+    W = synth.normal_bf16(gen, (V, H), w_std)
+    h = synth.normal_bf16(gen, (T, H), 1.0)
+    z = oracle.lm_head(bits_np(h), bits_np(W))
+    tg = torch.as_tensor(z.argmax(axis=1), dtype=torch.int64) if argmax_targets else \
+        synth.uniform_targets(gen, T, V)
+    g = torch.randn(T, generator=gen, dtype=torch.float32)
+    _, _, dh = _saved_fwd_bwd(rk, cuda(h), cuda(W), cuda(tg), cuda(g))
+    ref = oracle.linear_logp_bwd(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy())
+    chk = contract.check_gradient_accuracy(dh.cpu().numpy(), ref)
+    print(f"saved path, peaked w_std={w_std} argmax={argmax_targets}: {chk}")
+    assert chk.passed, chk
+    assert rk.get_device_error() == 0
+
+
+def test_saved_path_masking_and_bad_target(rk):
+    pool = synth.make_pool(128, 1500, [30, 50], seed=41, with_grad=True)
+    lay = synth.packed(pool, [0, 1], lead_pad=7)
+    tg = lay.targets.clone()
+    tg[20] = 1500                                   # out of range: NaN row + error bit
+    h, W, tgd, cu, g = cuda(lay.h), cuda(pool.W), cuda(tg), cuda(lay.cu_seqlens), cuda(lay.g)
+    rk.get_device_error()
+    _, _, dh = _saved_fwd_bwd(rk, h, W, tgd, g, cu)
+    assert rk.get_device_error() & rk.DEVERR_TARGET_RANGE
+    d = dh.cpu()
+    assert torch.all(d[:7] == 0) and torch.all(torch.isnan(d[20]))
+    ok = torch.ones(lay.T, dtype=torch.bool)
+    ok[20] = False
+    assert torch.all(torch.isfinite(d[ok]))
+    act = oracle.active_rows(tg.numpy(), lay.cu_seqlens.numpy()) & (tg.numpy() < 1500)
+    ref = oracle_bwd(bits_np(lay.h), bits_np(pool.W), np.where(act, tg.numpy(), -100),
+                     np.nan_to_num(lay.g.double().numpy()), lay.cu_seqlens.numpy())
+    assert contract.check_gradient_accuracy(d[ok].numpy(), ref[ok.numpy()]).passed
+
+
+def test_saved_path_invariance_tiny(rk):
+    # every transform class of the tiny workload: dh bitwise equal to the
+    # packed baseline on the logical rows
+    pool = synth.tiny_pool()
+    W = cuda(pool.W)
+
+    def run(lay):
+        h, tg, cu, g = cuda(lay.h), cuda(lay.targets), cuda(lay.cu_seqlens), cuda(lay.g)
+        logp, lse, dh = _saved_fwd_bwd(rk, h, W, tg, g, cu)
+        return {"logp": logp.cpu(), "lse": lse.cpu(), "dh": dh.cpu()}
+
+    base_lay = synth.packed(pool, [0, 1, 2, 3])
+    base = run(base_lay)
+    layouts = [(synth.packed(pool, [i]), [i]) for i in range(4)]
+    layouts += [(synth.packed(pool, [3, 2, 1, 0]), [0, 1, 2, 3]),
+                (synth.packed(pool, [0, 1, 2, 3], lead_pad=77), [0, 1, 2, 3]),
+                (synth.padded(pool, [0, 1, 2, 3], 40, side="left"), [0, 1, 2, 3]),
+                (synth.padded(pool, [0, 1, 2, 3], 160, side="right"), [0, 1, 2, 3]),
+                (synth.packed(synth.replace_neighbours(pool, [1], seed=synth.NEIGHBOUR_SEED_OFFSET),
+                              [0, 1, 2, 3]), [1])]
+    for lay, seqs in layouts:
+        out = run(lay)
+        for i in seqs:
+            b = torch.tensor(base_lay.rows_of[i])
+            v = torch.tensor(lay.rows_of[i])
+            for k in base:
+                assert torch.equal(out[k][v].view(torch.int32), base[k][b].view(torch.int32)), \
+                    (lay.description, i, k)
+    # the same physical batch twice: the same bits (the saved state is rebuilt)
+    again = run(base_lay)
+    assert all(same_bits(again[k], base[k]) for k in base)
+    assert rk.get_device_error() == 0
+
+
+@pytest.mark.slow
+def test_saved_path_grpo_sampled_rows(rk):
+    # the GRPO group at full size (T = 65536, H = 4096, V = 128256): sampled
+    # rows of dh against the oracle, and the decode-shaped launches (rows
+    # alone, T = 1 and 64) equal to the prefill rows bit for bit
+    pool = synth.grpo_pool()
+    lay = synth.packed(pool, list(range(len(pool.lengths))))
+    h, W, tg, g = cuda(lay.h), cuda(pool.W), cuda(lay.targets), cuda(lay.g)
+    logp, lse, dh = _saved_fwd_bwd(rk, h, W, tg, g)
+    assert rk.last_row_blocks("dh") == 2
+    rows = synth.sample_rows(lay.T, 64, seed=14)
+    ref = oracle_bwd(bits_np(lay.h), bits_np(pool.W), lay.targets.numpy(), lay.g.double().numpy(),
+                     rows=rows)
+    chk = contract.check_gradient_accuracy(dh.cpu()[rows].numpy(), ref)
+    print(f"saved path, grpo 64 sampled rows: dh {chk}")
+    assert chk.passed, chk
+    dh_c = dh.cpu()
+    for n in (1, 64):
+        sub = torch.arange(5000, 5000 + n, device=DEV)
+        _, _, dh1 = _saved_fwd_bwd(rk, h[sub].contiguous(), W, tg[sub].contiguous(),
+                                   g[sub].contiguous())
+        assert same_bits(dh1.cpu(), dh_c[5000:5000 + n]), n
+    assert rk.get_device_error() == 0
