@@ -29,6 +29,13 @@ constexpr int kConvGroupsPerThread = 4;
 constexpr int64_t kConvCols = (int64_t)kConvThreads * 8 * kConvGroupsPerThread;  // 8192 per block
 constexpr int kTileCols = 256;  // the forward's vocabulary tile
 
+// Elementwise max of two bf16 pairs (exact).
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 __device__ __noinline__ void list_entry(int64_t col, int32_t *count, int2 *list, unsigned *err) {
     const int slot = atomicAdd(count, 1);
     if (slot < kEntCap)
@@ -68,22 +75,34 @@ __global__ void __launch_bounds__(kConvThreads)
         const uint4 w = *gp;
         const uint32_t q[4] = {w.x, w.y, w.z, w.w};
         uint32_t o[4];
+        // The group's largest term decides, in one test, that no column of it
+        // needs an fp32 entry (f e <= f max(e) by the monotonic rounding of
+        // the product): the same decision as the per-column test below.
+        const uint32_t mx = max_bf16x2(max_bf16x2(q[0], q[1]), max_bf16x2(q[2], q[3]));
+        const bool plain = c0 + 8 <= V && !(tgt >= c0 && tgt < c0 + 8) &&
+                           __fmul_rn(f, fmaxf(bf16_lo(mx), bf16_hi(mx))) < kEntTau;
+        if (plain) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float d[2];
+            for (int k = 0; k < 4; ++k)
+                o[k] = pack_bf16x2(__fmul_rn(c, bf16_lo(q[k])), __fmul_rn(c, bf16_hi(q[k])));
+        } else {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int64_t col = c0 + 2 * k + hh;
-                const float e = hh ? bf16_hi(q[k]) : bf16_lo(q[k]);
-                d[hh] = 0.f;
-                if (col < V) {
-                    if (col == tgt || __fmul_rn(f, e) >= kEntTau)
-                        list_entry(col, ecount + row, ent + row * kEntCap, err);
-                    else
-                        d[hh] = __fmul_rn(c, e);
+            for (int k = 0; k < 4; ++k) {
+                float d[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int64_t col = c0 + 2 * k + hh;
+                    const float e = hh ? bf16_hi(q[k]) : bf16_lo(q[k]);
+                    d[hh] = 0.f;
+                    if (col < V) {
+                        if (col == tgt || __fmul_rn(f, e) >= kEntTau)
+                            list_entry(col, ecount + row, ent + row * kEntCap, err);
+                        else
+                            d[hh] = __fmul_rn(c, e);
+                    }
                 }
+                o[k] = pack_bf16x2(d[0], d[1]);
             }
-            o[k] = pack_bf16x2(d[0], d[1]);
         }
         *gp = make_uint4(o[0], o[1], o[2], o[3]);
     }
