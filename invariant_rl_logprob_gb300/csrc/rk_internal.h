@@ -165,14 +165,17 @@ cudaError_t launch_linear_bwd_saved(const uint16_t *h, const uint16_t *W, const 
                                     int64_t V, const float *lse, const float *grad, void *saved,
                                     float *dh, void *workspace, const DeviceInfo &di,
                                     cudaStream_t st);
+// The elementwise steps over rows [row0, row0 + rows).
 cudaError_t launch_stash_to_dz(uint16_t *dz, int64_t ldz, const float2 *part, int32_t num_n,
-                               const int64_t *targets, const int32_t *cu, int num_seqs, int64_t T,
-                               int64_t V, const float *lse, const float *grad, int32_t *ecount,
-                               int2 *ent, const DeviceInfo &di, cudaStream_t st);
+                               const int64_t *targets, const int32_t *cu, int num_seqs,
+                               int64_t row0, int64_t rows, int64_t V, const float *lse,
+                               const float *grad, int32_t *ecount, int2 *ent, const DeviceInfo &di,
+                               cudaStream_t st);
 cudaError_t launch_exact_entries(const uint16_t *h, const uint16_t *W, int64_t H,
-                                 const int64_t *targets, const int32_t *cu, int num_seqs, int64_t T,
-                                 int64_t V, const float *lse, const float *grad,
-                                 const int32_t *ecount, int2 *ent, cudaStream_t st);
+                                 const int64_t *targets, const int32_t *cu, int num_seqs,
+                                 int64_t row0, int64_t rows, int64_t V, const float *lse,
+                                 const float *grad, const int32_t *ecount, int2 *ent,
+                                 cudaStream_t st);
 
 // ---- linear_logp backward (linear_logp_tc.cu) ----
 size_t linear_bwd_chunk_bytes(int64_t rows, int64_t V);

@@ -44,16 +44,16 @@ __device__ __noinline__ void list_entry(int64_t col, int32_t *count, int2 *list,
         atomicOr(err, kErrLse);
 }
 
-// grid (T, ceil(V / kConvCols)): block (t, q) takes columns
-// [q kConvCols, (q + 1) kConvCols) of row t, 8 consecutive columns per thread
-// and group (a group of 8 never crosses a 256-column tile).
+// grid (rows, ceil(V / kConvCols)): block (r, q) takes columns
+// [q kConvCols, (q + 1) kConvCols) of row row0 + r, 8 consecutive columns per
+// thread and group (a group of 8 never crosses a 256-column tile).
 __global__ void __launch_bounds__(kConvThreads)
     stash_to_dz(uint16_t *__restrict__ dz, int64_t ldz, const float2 *__restrict__ part,
                 int32_t num_n, const int64_t *__restrict__ targets, const int32_t *__restrict__ cu,
-                int num_seqs, int64_t V, const float *__restrict__ lse,
+                int num_seqs, int64_t row0, int64_t V, const float *__restrict__ lse,
                 const float *__restrict__ grad, int32_t *__restrict__ ecount,
                 int2 *__restrict__ ent, unsigned *err) {
-    const int64_t row = blockIdx.x;
+    const int64_t row = row0 + blockIdx.x;
     const int64_t tgt = targets[row];
     const bool active = row_active(row, tgt, cu, num_seqs) && tgt < V;
     uint16_t *drow = dz + row * ldz;
@@ -115,12 +115,12 @@ constexpr int kExactRowsPerBlock = 8;
 __global__ void __launch_bounds__(32 * kExactRowsPerBlock)
     exact_entries(const uint16_t *__restrict__ h, const uint16_t *__restrict__ W, int64_t H,
                   const int64_t *__restrict__ targets, const int32_t *__restrict__ cu,
-                  int num_seqs, int64_t T, int64_t V, const float *__restrict__ lse,
-                  const float *__restrict__ grad, const int32_t *__restrict__ ecount,
-                  int2 *__restrict__ ent) {
-    const int64_t row = (int64_t)blockIdx.x * kExactRowsPerBlock + (threadIdx.x >> 5);
+                  int num_seqs, int64_t row0, int64_t row_end, int64_t V,
+                  const float *__restrict__ lse, const float *__restrict__ grad,
+                  const int32_t *__restrict__ ecount, int2 *__restrict__ ent) {
+    const int64_t row = row0 + (int64_t)blockIdx.x * kExactRowsPerBlock + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (row >= T) return;
+    if (row >= row_end) return;
     const int64_t tgt = targets[row];
     if (!row_active(row, tgt, cu, num_seqs) || tgt >= V) return;
     const int n = min(ecount[row], kEntCap);
@@ -152,26 +152,28 @@ __global__ void __launch_bounds__(32 * kExactRowsPerBlock)
 }  // namespace
 
 cudaError_t launch_stash_to_dz(uint16_t *dz, int64_t ldz, const float2 *part, int32_t num_n,
-                               const int64_t *targets, const int32_t *cu, int num_seqs, int64_t T,
-                               int64_t V, const float *lse, const float *grad, int32_t *ecount,
-                               int2 *ent, const DeviceInfo &di, cudaStream_t st) {
-    if (T == 0) return cudaSuccess;
+                               const int64_t *targets, const int32_t *cu, int num_seqs,
+                               int64_t row0, int64_t rows, int64_t V, const float *lse,
+                               const float *grad, int32_t *ecount, int2 *ent, const DeviceInfo &di,
+                               cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
     const int64_t segs = (V + kConvCols - 1) / kConvCols;
     if (segs > 65535) return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)T, (unsigned)segs);
-    stash_to_dz<<<grid, kConvThreads, 0, st>>>(dz, ldz, part, num_n, targets, cu, num_seqs, V, lse,
-                                              grad, ecount, ent, di.err);
+    const dim3 grid((unsigned)rows, (unsigned)segs);
+    stash_to_dz<<<grid, kConvThreads, 0, st>>>(dz, ldz, part, num_n, targets, cu, num_seqs, row0, V,
+                                              lse, grad, ecount, ent, di.err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_exact_entries(const uint16_t *h, const uint16_t *W, int64_t H,
-                                 const int64_t *targets, const int32_t *cu, int num_seqs, int64_t T,
-                                 int64_t V, const float *lse, const float *grad,
-                                 const int32_t *ecount, int2 *ent, cudaStream_t st) {
-    if (T == 0) return cudaSuccess;
-    const unsigned grid = (unsigned)((T + kExactRowsPerBlock - 1) / kExactRowsPerBlock);
-    exact_entries<<<grid, 32 * kExactRowsPerBlock, 0, st>>>(h, W, H, targets, cu, num_seqs, T, V,
-                                                           lse, grad, ecount, ent);
+                                 const int64_t *targets, const int32_t *cu, int num_seqs,
+                                 int64_t row0, int64_t rows, int64_t V, const float *lse,
+                                 const float *grad, const int32_t *ecount, int2 *ent,
+                                 cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)((rows + kExactRowsPerBlock - 1) / kExactRowsPerBlock);
+    exact_entries<<<grid, 32 * kExactRowsPerBlock, 0, st>>>(h, W, H, targets, cu, num_seqs, row0,
+                                                           row0 + rows, V, lse, grad, ecount, ent);
     return cudaGetLastError();
 }
 
