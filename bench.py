@@ -396,7 +396,24 @@ def measure_rows(rk, pool, zs, peaks, dev, stream) -> dict:
                                    "peak": peaks["bf16_tflops_sustained"],
                                    "frac": tf / peaks["bf16_tflops_sustained"],
                                    "algorithmic": "6*T*H*V flop (dZ + dh + dW GEMMs)"}
-    del wsd, dW, dh
+    # the same from the forward's saved terms (read only): dZ converted, not
+    # recomputed; the forward that keeps them is timed with it: 6*T*H*V flop
+    # of GEMMs in the recompute form against 4*T*H*V here (fwd, dh, dW)
+    saved = torch.empty(rk.linear_logp_saved_size(T, H, V), dtype=torch.uint8, device=dev)
+
+    def full_saved(i):
+        rk.linear_logp_fwd_saved(h, W, tg, lse=lse, saved=saved, stream=stream)
+        rk.linear_logp_bwd_full_saved(h, W, tg, lse, g, saved, dh=dh, dW=dW, workspace=wsd,
+                                      stream=stream)
+    ms = time_loop(full_saved, 3, stream)
+    tf = 6.0 * T * H * V / (ms / 1e3) / 1e12
+    out["linear_logp_fwd_bwd_full_saved"] = {
+        "shape": [T, H, V], "ms_per_call": ms, "tokens_per_s": T / (ms / 1e3), "bound": "tensor",
+        "achieved_equiv": tf, "unit": "TFLOP/s",
+        "algorithmic": "forward + dh + dW: 6*T*H*V flop of GEMMs in the recompute form, 4*T*H*V "
+                       "in this one (no dZ GEMM); achieved_equiv counts 6*T*H*V",
+        "note": "compare with linear_logp_bwd_full (backward alone, recompute) + the forward"}
+    del wsd, dW, dh, saved
     # the backward that recomputes z with a second GEMM (no saved terms):
     # forward + backward, 6*T*H*V flop
     wsf = torch.empty(rk.linear_logp_workspace_size(T, H, V), dtype=torch.uint8, device=dev)

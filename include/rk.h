@@ -365,6 +365,28 @@ rk_status rk_linear_logp_bwd_full(const uint16_t *h, const uint16_t *W, const in
                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * rk_linear_logp_bwd_full from the forward's saved terms: dh and dW of the
+ * same canonical tokens, with dZ converted from `saved` (as
+ * rk_linear_logp_bwd_saved converts it) instead of recomputed, so the call
+ * runs two GEMMs (dh, dW) instead of three.  dh is bitwise that of
+ * rk_linear_logp_bwd_saved on the same saved state; dW is bitwise the same
+ * for the same tokens in the same canonical order, whatever their layout, and
+ * within the gradient tolerance of rk_linear_logp_dw.  `saved` is only read
+ * (it can serve this call and then rk_linear_logp_bwd_saved, or be reused).
+ *   arguments: as rk_linear_logp_bwd_full, plus saved / saved_bytes from
+ *   rk_linear_logp_fwd_saved on the same h, W, targets, cu_seqlens (same T);
+ *   workspace >= rk_linear_logp_bwd_full_workspace_size(n, H, V) bytes.
+ */
+rk_status rk_linear_logp_bwd_full_saved(const uint16_t *h, const uint16_t *W,
+                                        const int64_t *targets, const int32_t *cu_seqlens,
+                                        int32_t num_seqs, int64_t T, int64_t H, int64_t V,
+                                        const float *lse, const float *grad_logp,
+                                        const void *saved, size_t saved_bytes,
+                                        const int64_t *row_order, int64_t n_order,
+                                        float *dh, float *dW,
+                                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * rk_linear_logp without a workspace argument, for callers that cannot
  * allocate device memory.  (No counterpart in the pages: this is an interface
  * convenience, not part of the method.)  Such callers include programs whose

@@ -29,7 +29,7 @@ __all__ = [
     "linear_logp_bwd", "linear_logp_bwd_workspace_size", "linear_logp_bwd_min_workspace_size",
     "lm_head", "logp_from_logits_bwd", "grpo_token_loss", "linear_logp_grpo", "linear_greedy",
     "linear_logp_fwd_saved", "linear_logp_bwd_saved", "linear_logp_saved_size",
-    "linear_logp_bwd_saved_workspace_size",
+    "linear_logp_bwd_saved_workspace_size", "linear_logp_bwd_full_saved",
     "linear_greedy_workspace_size", "linear_logp_dw", "linear_logp_dw_workspace_size",
     "linear_logp_bwd_full", "linear_logp_bwd_full_workspace_size", "lm_head_workspace_size",
     "get_device_error", "selftest_wait_timeout", "set_row_blocks", "last_row_blocks", "DEVERR_TARGET_RANGE", "DEVERR_TIMEOUT", "DEVERR_LSE",
@@ -130,6 +130,9 @@ def load_library() -> ctypes.CDLL:
     lib.rk_linear_logp_bwd_saved.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, sz, vp,
                                              vp, sz, vp]
     lib.rk_linear_logp_bwd_saved.restype = ctypes.c_int
+    lib.rk_linear_logp_bwd_full_saved.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp,
+                                                  sz, vp, i64, vp, vp, vp, sz, vp]
+    lib.rk_linear_logp_bwd_full_saved.restype = ctypes.c_int
     lib.rk_set_row_blocks.argtypes = [i32]
     lib.rk_set_row_blocks.restype = ctypes.c_int
     lib.rk_last_row_blocks.argtypes = [i32]
@@ -441,6 +444,42 @@ def linear_logp_bwd_saved(h: torch.Tensor, W: torch.Tensor, targets: torch.Tenso
                                       _stream_handle(stream, h.device))
     _check(st, "rk_linear_logp_bwd_saved")
     return dh
+
+
+def linear_logp_bwd_full_saved(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor,
+                               lse: torch.Tensor, grad_logp: torch.Tensor, saved: torch.Tensor,
+                               cu_seqlens: torch.Tensor | None = None, *,
+                               row_order: torch.Tensor | None = None,
+                               dh: torch.Tensor | None = None, dW: torch.Tensor | None = None,
+                               workspace: torch.Tensor | None = None,
+                               stream: torch.cuda.Stream | None = None):
+    """(dh fp32 [T, H], dW fp32 [V, H]) from the state :func:`linear_logp_fwd_saved`
+    kept (read only)."""
+    lib = load_library()
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    T, H = h.shape
+    V = W.shape[0]
+    cu, ns = _rows(targets, cu_seqlens, T, h.device)
+    if row_order is not None:
+        _need(row_order, "row_order", torch.int64, 1)
+        n = row_order.shape[0]
+    else:
+        n = T
+    if dh is None:
+        dh = torch.empty((T, H), dtype=torch.float32, device=h.device)
+    if dW is None:
+        dW = torch.empty((V, H), dtype=torch.float32, device=h.device)
+    if workspace is None:
+        need = int(lib.rk_linear_logp_bwd_full_workspace_size(n, H, V))
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
+    st = lib.rk_linear_logp_bwd_full_saved(_ptr(h), _ptr(W), _ptr(targets), _ptr(cu), ns, T, H, V,
+                                           _ptr(lse), _ptr(grad_logp), _ptr(saved), saved.numel(),
+                                           _ptr(row_order), n, _ptr(dh), _ptr(dW),
+                                           _ptr(workspace), workspace.numel(),
+                                           _stream_handle(stream, h.device))
+    _check(st, "rk_linear_logp_bwd_full_saved")
+    return dh, dW
 
 
 def linear_greedy_workspace_size(T: int, H: int, V: int) -> int:

@@ -1424,7 +1424,8 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
                                       const int32_t *cu, int num_seqs, int64_t T, int64_t H,
                                       int64_t V, const float *lse, const float *grad,
                                       const int64_t *order, int64_t n, float *dh, float *dW,
-                                      void *workspace, const DeviceInfo &di, cudaStream_t st);
+                                      void *workspace, const DeviceInfo &di, cudaStream_t st,
+                                      const void *saved = nullptr);
 
 cudaError_t launch_linear_dw(const uint16_t *h, const uint16_t *W, const int64_t *targets,
                              const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
@@ -1438,12 +1439,12 @@ cudaError_t launch_linear_bwd_full(const uint16_t *h, const uint16_t *W, const i
                                    const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
                                    const float *lse, const float *grad, const int64_t *order,
                                    int64_t n, float *dh, float *dW, void *workspace,
-                                   const DeviceInfo &di, cudaStream_t st) {
+                                   const DeviceInfo &di, cudaStream_t st, const void *saved) {
     // rows outside the canonical set keep dh = 0; out-of-range targets get NaN
     cudaError_t e = cudaMemsetAsync(dh, 0, (size_t)T * (size_t)H * sizeof(float), st);
     if (e != cudaSuccess) return e;
     e = canonical_backward(h, W, targets, cu, num_seqs, T, H, V, lse, grad, order, n, dh, dW,
-                           workspace, di, st);
+                           workspace, di, st, saved);
     if (e != cudaSuccess) return e;
     if (T > 0) {
         linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(targets, cu, num_seqs, T,
@@ -1457,7 +1458,9 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
                                       const int32_t *cu, int num_seqs, int64_t T, int64_t H,
                                       int64_t V, const float *lse, const float *grad,
                                       const int64_t *order, int64_t n, float *dh, float *dW,
-                                      void *workspace, const DeviceInfo &di, cudaStream_t st) {
+                                      void *workspace, const DeviceInfo &di, cudaStream_t st,
+                                      const void *saved) {
+    if (saved && !dh) return cudaErrorInvalidValue;  // the saved form is the full backward
     if (n == 0)
         return dW ? cudaMemsetAsync(dW, 0, (size_t)V * (size_t)H * sizeof(float), st) : cudaSuccess;
     uint8_t *w = reinterpret_cast<uint8_t *>(workspace);
@@ -1567,12 +1570,6 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
         return run_dw();
     }
 
-    // dZ over the canonical tokens (every position past the active count has
-    // target -1 and so gives a zero row)
-    if (!encode_tmap_bf16_2d(&tmHc, bf.hc, (uint64_t)H, (uint64_t)n, (uint64_t)H * 2, BK, BM, true))
-        return cudaErrorInvalidValue;
-    if (!encode_tmap_bf16_2d(&tmW, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2, true))
-        return cudaErrorInvalidValue;
     TileArgs a{};
     a.tile_counter = counter;
     a.targets = bf.tgtc;
@@ -1592,21 +1589,47 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
     a.num_m = (int32_t)((n + 2 * BM - 1) / (2 * BM));
     a.num_n = (int32_t)((V + BN - 1) / BN);
     a.num_k = (int32_t)(H / BK);
-    // dZ^T as well, through 32 x 32 TMA stores from the epilogue
-    CUtensorMap tmDzTs;
-    if (!encode_tmap_bf16_2d(&tmDzTs, dzT, (uint64_t)n, (uint64_t)V, (uint64_t)ldn * 2, 32, 32,
-                             false))
-        return cudaErrorInvalidValue;
-    CUtensorMap tmDzS;
-    if (!encode_tmap_bf16_2d_sw64(&tmDzS, bf.dz, (uint64_t)V, (uint64_t)n, (uint64_t)bf.ldz * 2, 32,
-                                  32))
-        return cudaErrorInvalidValue;
-    a.dzT_store = true;
-    a.dz_tma = true;
-    e = run_tiles<kDz>(tmHc, tmW, a, di, st, &tmDzTs, &tmDzS);
-    if (e != cudaSuccess) return e;
-    a.dzT_store = false;
-    a.dz_tma = false;
+    if (saved) {
+        // dZ over the canonical tokens from the forward's saved terms (the
+        // same conversion as rk_linear_logp_bwd_saved, so the same bits), the
+        // entries' fp32 weights from an exact z; dZ^T by a transpose
+        const uint8_t *sv = reinterpret_cast<const uint8_t *>(saved);
+        const float2 *part = reinterpret_cast<const float2 *>(sv);
+        const uint16_t *terms = reinterpret_cast<const uint16_t *>(sv + linear_fwd_workspace_bytes(T, V));
+        e = launch_stash_to_dz_canonical(terms, bf.ldz, part, (int32_t)((V + BN - 1) / BN), bf.crow,
+                                         bf.n_active, bf.tgtc, bf.lsec, bf.gc, n, V, bf.dz,
+                                         bf.ecount, bf.ent, di, st);
+        if (e != cudaSuccess) return e;
+        e = launch_exact_entries(bf.hc, W, H, bf.tgtc, nullptr, 0, 0, n, V, bf.lsec, bf.gc,
+                                 bf.ecount, bf.ent, st);
+        if (e != cudaSuccess) return e;
+        e = launch_transpose_dz(bf.dz, bf.ldz, n, V, dzT, ldn, st);
+        if (e != cudaSuccess) return e;
+    } else {
+        // dZ over the canonical tokens (every position past the active count
+        // has target -1 and so gives a zero row), dZ^T as well, through 32 x 32
+        // TMA stores from the epilogue
+        if (!encode_tmap_bf16_2d(&tmHc, bf.hc, (uint64_t)H, (uint64_t)n, (uint64_t)H * 2, BK, BM,
+                                 true))
+            return cudaErrorInvalidValue;
+        if (!encode_tmap_bf16_2d(&tmW, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2,
+                                 true))
+            return cudaErrorInvalidValue;
+        CUtensorMap tmDzTs;
+        if (!encode_tmap_bf16_2d(&tmDzTs, dzT, (uint64_t)n, (uint64_t)V, (uint64_t)ldn * 2, 32, 32,
+                                 false))
+            return cudaErrorInvalidValue;
+        CUtensorMap tmDzS;
+        if (!encode_tmap_bf16_2d_sw64(&tmDzS, bf.dz, (uint64_t)V, (uint64_t)n, (uint64_t)bf.ldz * 2,
+                                      32, 32))
+            return cudaErrorInvalidValue;
+        a.dzT_store = true;
+        a.dz_tma = true;
+        e = run_tiles<kDz>(tmHc, tmW, a, di, st, &tmDzTs, &tmDzS);
+        if (e != cudaSuccess) return e;
+        a.dzT_store = false;
+        a.dz_tma = false;
+    }
 
     if (dh) {
         // dh over the canonical rows, K = V ascending, each row stored at its

@@ -502,6 +502,45 @@ int32_t rk_last_row_blocks(int32_t gemm) {
     return (int32_t)rk::last_row_blocks(gemm == 0 ? rk::RowGemm::kDhGemm : rk::RowGemm::kDwGemm);
 }
 
+rk_status rk_linear_logp_bwd_full_saved(const uint16_t *h, const uint16_t *W,
+                                        const int64_t *targets, const int32_t *cu_seqlens,
+                                        int32_t num_seqs, int64_t T, int64_t H, int64_t V,
+                                        const float *lse, const float *grad_logp,
+                                        const void *saved, size_t saved_bytes,
+                                        const int64_t *row_order, int64_t n_order, float *dh,
+                                        float *dW, void *workspace, size_t workspace_bytes,
+                                        void *stream) {
+    if (T < 0 || H <= 0 || V <= 0) return RK_ERR_INVALID_ARG;
+    if (!dW || !W || (T > 0 && !dh)) return RK_ERR_INVALID_ARG;
+    const int64_t n = row_order ? n_order : T;
+    if (n < 0) return RK_ERR_INVALID_ARG;
+    if ((n > 0 || T > 0) && (!h || !lse || !grad_logp)) return RK_ERR_INVALID_ARG;
+    if (T > 0 || n > 0) {
+        rk_status st = check_rows(targets, cu_seqlens, num_seqs);
+        if (st != RK_OK) return st;
+    }
+    if (H % 64 != 0 || H > 65536 || V >= (int64_t(1) << 31) || T >= (int64_t(1) << 31) ||
+        n >= (int64_t(1) << 31))
+        return RK_ERR_UNSUPPORTED;
+    if ((V + 8191) / 8192 > 65535 || (V + 63) / 64 > 65535) return RK_ERR_UNSUPPORTED;
+    if ((h && !aligned(h, 16)) || !aligned(W, 16) || !aligned(dW, 16) || (dh && !aligned(dh, 16)))
+        return RK_ERR_UNSUPPORTED;
+    if (T > 0 && (!saved || saved_bytes < rk::linear_fwd_saved_bytes(T, V)))
+        return RK_ERR_WORKSPACE;
+    if (saved && !aligned(saved, 256)) return RK_ERR_INVALID_ARG;
+    if (n > 0 && (!workspace || workspace_bytes < rk::linear_bwd_full_workspace_bytes(n, H, V)))
+        return RK_ERR_WORKSPACE;
+    if (n > 0 && !aligned(workspace, 16)) return RK_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = rk::current_device_info(&di);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    e = rk::launch_linear_bwd_full(h, W, targets, cu_seqlens, num_seqs, T, H, V, lse, grad_logp,
+                                   row_order, n, dh, dW, workspace, di,
+                                   static_cast<cudaStream_t>(stream), T > 0 ? saved : nullptr);
+    if (e != cudaSuccess) return rk::cuda_fail(e);
+    return RK_OK;
+}
+
 rk_status rk_selftest_wait_timeout(int64_t limit_ns, void *stream) {
     if (limit_ns <= 0 || limit_ns > 10000000000ll) return RK_ERR_INVALID_ARG;
     DeviceInfo di;

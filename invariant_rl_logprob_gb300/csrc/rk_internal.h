@@ -138,11 +138,14 @@ cudaError_t launch_linear_dw(const uint16_t *h, const uint16_t *W, const int64_t
                              const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
                              const float *lse, const float *grad, const int64_t *order, int64_t n,
                              float *dW, void *workspace, const DeviceInfo &di, cudaStream_t st);
+// With `saved` (the state of launch_linear_fwd_saved; read only), dZ comes
+// from the saved terms instead of a z recompute.
 cudaError_t launch_linear_bwd_full(const uint16_t *h, const uint16_t *W, const int64_t *targets,
                                    const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
                                    const float *lse, const float *grad, const int64_t *order,
                                    int64_t n, float *dh, float *dW, void *workspace,
-                                   const DeviceInfo &di, cudaStream_t st);
+                                   const DeviceInfo &di, cudaStream_t st,
+                                   const void *saved = nullptr);
 
 // ---- dh / dW GEMM form (linear_logp_tc.cu) ----
 // Both GEMMs run with one or two 256-row blocks per tile; the form never
@@ -171,6 +174,15 @@ cudaError_t launch_stash_to_dz(uint16_t *dz, int64_t ldz, const float2 *part, in
                                int64_t row0, int64_t rows, int64_t V, const float *lse,
                                const float *grad, int32_t *ecount, int2 *ent, const DeviceInfo &di,
                                cudaStream_t st);
+// Conversion into canonical order (the dW backward) and dZ -> dZ^T.
+cudaError_t launch_stash_to_dz_canonical(const uint16_t *terms, int64_t ldz, const float2 *part,
+                                         int32_t num_n, const int64_t *crow,
+                                         const int64_t *n_active, const int64_t *tgtc,
+                                         const float *lsec, const float *gc, int64_t n, int64_t V,
+                                         uint16_t *dzc, int32_t *ecount, int2 *ent,
+                                         const DeviceInfo &di, cudaStream_t st);
+cudaError_t launch_transpose_dz(const uint16_t *dz, int64_t ldz, int64_t n, int64_t V,
+                                uint16_t *dzt, int64_t ldn, cudaStream_t st);
 cudaError_t launch_exact_entries(const uint16_t *h, const uint16_t *W, int64_t H,
                                  const int64_t *targets, const int32_t *cu, int num_seqs,
                                  int64_t row0, int64_t rows, int64_t V, const float *lse,

@@ -12,6 +12,9 @@
 //                 every column except the target and the columns with
 //                 p >= 1/64, which it leaves as 0 and lists as the row's fp32
 //                 entries (as the recompute path does);
+//   stash_to_dz_canonical does the same for the canonical tokens of the dW
+//                 backward, writing dZ in canonical order (transpose_dz then
+//                 gives the dW GEMM its dZ^T);
 //   exact_entries gives each listed column its fp32 weight
 //                 w = g (onehot - p) from an exact z = h_t . W_v (fp32, one
 //                 fixed order), so a peaked softmax never puts a rounded large
@@ -44,6 +47,50 @@ __device__ __noinline__ void list_entry(int64_t col, int32_t *count, int2 *list,
         atomicOr(err, kErrLse);
 }
 
+// One group of 8 saved terms (columns [c0, c0 + 8) of a row with lse l,
+// gradient g and target tgt, in the tile whose maximum is mt) -> dZ, with
+// the target and p >= 1/64 columns left at 0 and listed.  The one function
+// both conversion kernels use, so a row's dZ and entries do not depend on
+// which of them ran.
+__device__ __forceinline__ uint4 convert_group(uint4 w, int64_t c0, int64_t V, int64_t tgt, float mt,
+                                               float l, float g, int32_t *count, int2 *list,
+                                               unsigned *err) {
+    const float f = ex2(__fmul_rn(__fsub_rn(mt, l), kLog2e));  // e^(m_tj - lse) <= 1
+    const float c = __fmul_rn(g, f);
+    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+    uint32_t o[4];
+    // The group's largest term decides, in one test, that no column of it
+    // needs an fp32 entry (f e <= f max(e) by the monotonic rounding of the
+    // product): the same decision as the per-column test below.
+    const uint32_t mx = max_bf16x2(max_bf16x2(q[0], q[1]), max_bf16x2(q[2], q[3]));
+    const bool plain = c0 + 8 <= V && !(tgt >= c0 && tgt < c0 + 8) &&
+                       __fmul_rn(f, fmaxf(bf16_lo(mx), bf16_hi(mx))) < kEntTau;
+    if (plain) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            o[k] = pack_bf16x2(__fmul_rn(c, bf16_lo(q[k])), __fmul_rn(c, bf16_hi(q[k])));
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float d[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int64_t col = c0 + 2 * k + hh;
+                const float e = hh ? bf16_hi(q[k]) : bf16_lo(q[k]);
+                d[hh] = 0.f;
+                if (col < V) {
+                    if (col == tgt || __fmul_rn(f, e) >= kEntTau)
+                        list_entry(col, count, list, err);
+                    else
+                        d[hh] = __fmul_rn(c, e);
+                }
+            }
+            o[k] = pack_bf16x2(d[0], d[1]);
+        }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // grid (rows, ceil(V / kConvCols)): block (r, q) takes columns
 // [q kConvCols, (q + 1) kConvCols) of row row0 + r, 8 consecutive columns per
 // thread and group (a group of 8 never crosses a 256-column tile).
@@ -69,42 +116,65 @@ __global__ void __launch_bounds__(kConvThreads)
             *gp = make_uint4(0, 0, 0, 0);
             continue;
         }
-        const float mt = part[row * num_n + c0 / kTileCols].x;
-        const float f = ex2(__fmul_rn(__fsub_rn(mt, l), kLog2e));  // e^(m_tj - lse) <= 1
-        const float c = __fmul_rn(g, f);
-        const uint4 w = *gp;
-        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
-        uint32_t o[4];
-        // The group's largest term decides, in one test, that no column of it
-        // needs an fp32 entry (f e <= f max(e) by the monotonic rounding of
-        // the product): the same decision as the per-column test below.
-        const uint32_t mx = max_bf16x2(max_bf16x2(q[0], q[1]), max_bf16x2(q[2], q[3]));
-        const bool plain = c0 + 8 <= V && !(tgt >= c0 && tgt < c0 + 8) &&
-                           __fmul_rn(f, fmaxf(bf16_lo(mx), bf16_hi(mx))) < kEntTau;
-        if (plain) {
+        *gp = convert_group(*gp, c0, V, tgt, part[row * num_n + c0 / kTileCols].x, l, g,
+                            ecount + row, ent + row * kEntCap, err);
+    }
+}
+
+// The same conversion into canonical order: canonical token c (physical row
+// crow[c], c < n_active; later positions are zero rows) takes the saved terms
+// of its row and writes dZ row c of dzc and entry list c.  The row's lse, g
+// and target come from the canonical copies.
+__global__ void __launch_bounds__(kConvThreads)
+    stash_to_dz_canonical(const uint16_t *__restrict__ terms, int64_t ldz,
+                          const float2 *__restrict__ part, int32_t num_n,
+                          const int64_t *__restrict__ crow, const int64_t *__restrict__ n_active,
+                          const int64_t *__restrict__ tgtc, const float *__restrict__ lsec,
+                          const float *__restrict__ gc, int64_t V, uint16_t *__restrict__ dzc,
+                          int32_t *__restrict__ ecount, int2 *__restrict__ ent, unsigned *err) {
+    const int64_t c = blockIdx.x;
+    const bool live = c < *n_active;
+    const int64_t row = live ? crow[c] : 0;
+    const int64_t tgt = live ? tgtc[c] : -1;
+    uint16_t *drow = dzc + c * ldz;
+    const uint16_t *srow = terms + row * ldz;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                o[k] = pack_bf16x2(__fmul_rn(c, bf16_lo(q[k])), __fmul_rn(c, bf16_hi(q[k])));
-        } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                float d[2];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int64_t col = c0 + 2 * k + hh;
-                    const float e = hh ? bf16_hi(q[k]) : bf16_lo(q[k]);
-                    d[hh] = 0.f;
-                    if (col < V) {
-                        if (col == tgt || __fmul_rn(f, e) >= kEntTau)
-                            list_entry(col, ecount + row, ent + row * kEntCap, err);
-                        else
-                            d[hh] = __fmul_rn(c, e);
-                    }
-                }
-                o[k] = pack_bf16x2(d[0], d[1]);
-            }
+    for (int i = 0; i < kConvGroupsPerThread; ++i) {
+        const int64_t c0 = (int64_t)blockIdx.y * kConvCols + (int64_t)i * (kConvThreads * 8) +
+                           (int64_t)threadIdx.x * 8;
+        if (c0 >= V) continue;
+        uint4 *gp = reinterpret_cast<uint4 *>(drow + c0);
+        if (!live) {
+            *gp = make_uint4(0, 0, 0, 0);
+            continue;
         }
-        *gp = make_uint4(o[0], o[1], o[2], o[3]);
+        *gp = convert_group(*reinterpret_cast<const uint4 *>(srow + c0), c0, V, tgt,
+                            part[row * num_n + c0 / kTileCols].x, lsec[c], gc[c], ecount + c,
+                            ent + c * kEntCap, err);
+    }
+}
+
+// dZ^T [V][ldn] from dZ [n][ldz] (bf16), through 64 x 64 tiles in shared
+// memory; token columns in [n, ldn) are written as 0.
+constexpr int kTrTile = 64;
+__global__ void __launch_bounds__(256)
+    transpose_dz(const uint16_t *__restrict__ dz, int64_t ldz, int64_t n, int64_t V,
+                 uint16_t *__restrict__ dzt, int64_t ldn) {
+    __shared__ uint16_t tile[kTrTile][kTrTile + 2];
+    const int tx = threadIdx.x % kTrTile, ty = threadIdx.x / kTrTile;  // 64 x 4
+    const int64_t t0 = (int64_t)blockIdx.x * kTrTile, v0 = (int64_t)blockIdx.y * kTrTile;
+#pragma unroll
+    for (int j = 0; j < kTrTile / 4; ++j) {
+        const int r = ty + 4 * j;
+        const int64_t t = t0 + r, v = v0 + tx;
+        tile[r][tx] = (t < n && v < V) ? dz[t * ldz + v] : (uint16_t)0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kTrTile / 4; ++j) {
+        const int r = ty + 4 * j;
+        const int64_t v = v0 + r, t = t0 + tx;
+        if (v < V && t < ldn) dzt[v * ldn + t] = tile[tx][r];
     }
 }
 
@@ -162,6 +232,32 @@ cudaError_t launch_stash_to_dz(uint16_t *dz, int64_t ldz, const float2 *part, in
     const dim3 grid((unsigned)rows, (unsigned)segs);
     stash_to_dz<<<grid, kConvThreads, 0, st>>>(dz, ldz, part, num_n, targets, cu, num_seqs, row0, V,
                                               lse, grad, ecount, ent, di.err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stash_to_dz_canonical(const uint16_t *terms, int64_t ldz, const float2 *part,
+                                         int32_t num_n, const int64_t *crow,
+                                         const int64_t *n_active, const int64_t *tgtc,
+                                         const float *lsec, const float *gc, int64_t n, int64_t V,
+                                         uint16_t *dzc, int32_t *ecount, int2 *ent,
+                                         const DeviceInfo &di, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int64_t segs = (V + kConvCols - 1) / kConvCols;
+    if (segs > 65535) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)n, (unsigned)segs);
+    stash_to_dz_canonical<<<grid, kConvThreads, 0, st>>>(terms, ldz, part, num_n, crow, n_active,
+                                                        tgtc, lsec, gc, V, dzc, ecount, ent,
+                                                        di.err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_dz(const uint16_t *dz, int64_t ldz, int64_t n, int64_t V,
+                                uint16_t *dzt, int64_t ldn, cudaStream_t st) {
+    if (n == 0 || V == 0) return cudaSuccess;
+    const int64_t gy = (V + kTrTile - 1) / kTrTile;
+    if (gy > 65535) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)((ldn + kTrTile - 1) / kTrTile), (unsigned)gy);
+    transpose_dz<<<grid, 256, 0, st>>>(dz, ldz, n, V, dzt, ldn);
     return cudaGetLastError();
 }
 

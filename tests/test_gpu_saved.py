@@ -148,3 +148,77 @@ def test_saved_path_grpo_sampled_rows(rk):
                                    g[sub].contiguous())
         assert same_bits(dh1.cpu(), dh_c[5000:5000 + n]), n
     assert rk.get_device_error() == 0
+
+
+# --------------------------------------------------------------------------
+# dh and dW together from the saved terms (rk_linear_logp_bwd_full_saved)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,H,V,kind", [(300, 128, 1001, "uniform"), (700, 256, 2001, "masked"),
+                                        (600, 256, 128256, "zipf"), (512, 512, 4096, "peaked")])
+def test_saved_full_backward_vs_oracle(rk, T, H, V, kind):
+    gen = synth.generator(8500 + T + V)
+    W = synth.normal_bf16(gen, (V, H), 0.25 if kind == "peaked" else 0.05)
+    h = synth.normal_bf16(gen, (T, H), 1.0)
+    tg = synth.uniform_targets(gen, T, V)
+    if kind == "zipf":
+        p = np.arange(1, V + 1, dtype=np.float64) ** -1.1
+        tg = torch.as_tensor(np.random.default_rng(85).choice(V, size=T, p=p / p.sum()))
+    if kind == "masked":
+        tg[::7] = -100
+    g = torch.randn(T, generator=gen, dtype=torch.float32)
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    _, lse, saved = rk.linear_logp_fwd_saved(hd, Wd, tgd)
+    dh, dW = rk.linear_logp_bwd_full_saved(hd, Wd, tgd, lse, gd, saved)
+    # dh is the saved-terms backward's, bit for bit (that call consumes `saved`)
+    dh_s = rk.linear_logp_bwd_saved(hd, Wd, tgd, lse, gd, saved)
+    assert same_bits(dh, dh_s)
+    from tests.helpers import oracle_dw
+    ref = oracle_dw(bits_np(h), bits_np(W), tg.numpy(), g.double().numpy())
+    chk = contract.check_gradient_accuracy(dW.cpu().numpy(), ref)
+    print(f"saved full backward dW T={T} V={V} {kind}: {chk}")
+    assert chk.passed, chk
+    assert rk.get_device_error() == 0
+
+
+def test_saved_full_backward_layout_invariance(rk):
+    # the same sample set in packed, padded and permuted layouts, each named
+    # in canonical (sequence, position) order: dW bitwise equal
+    pool = synth.make_pool(128, 3000, [40, 70, 25, 33], seed=91, with_grad=True)
+    W = cuda(pool.W)
+    seqs = [0, 1, 2, 3]
+
+    def dw_of(lay):
+        order = torch.tensor([r for i in seqs for r in lay.rows_of[i]], dtype=torch.int64)
+        h, tg, g = cuda(lay.h), cuda(lay.targets), cuda(lay.g)
+        _, lse, saved = rk.linear_logp_fwd_saved(h, W, tg)
+        return rk.linear_logp_bwd_full_saved(h, W, tg, lse, g, saved, row_order=cuda(order))[1].cpu()
+
+    base = dw_of(synth.packed(pool, seqs))
+    for lay in (synth.padded(pool, seqs, 80, side="right"), synth.padded(pool, seqs, 80, side="left"),
+                synth.packed(pool, [3, 2, 1, 0], lead_pad=37), synth.packed(pool, [2, 0, 3, 1])):
+        assert same_bits(dw_of(lay), base), lay.description
+    assert rk.get_device_error() == 0
+
+
+@pytest.mark.slow
+def test_saved_full_backward_grpo(rk):
+    # full size: dW within the tolerance of the recompute path's dW, the
+    # projection identity with dh, and dh bitwise the saved-terms backward's
+    from tests.test_gpu_dw import _projection_identity
+    pool = synth.grpo_pool()
+    h, W, tg, g = cuda(pool.h), cuda(pool.W), cuda(pool.targets), cuda(pool.g)
+    _, lse, saved = rk.linear_logp_fwd_saved(h, W, tg)
+    dh, dW = rk.linear_logp_bwd_full_saved(h, W, tg, lse, g, saved)
+    assert rk.last_row_blocks("dw") == 2
+    rel = _projection_identity(h, W, dh, dW)
+    print(f"saved full backward, GRPO projection identity residual {rel:.3g}")
+    assert rel < 1e-4, rel
+    dW_r = rk.linear_logp_dw(h, W, tg, lse, g)
+    chk = contract.check_gradient_accuracy(dW.cpu().numpy(), dW_r.double().cpu().numpy())
+    print(f"saved full backward dW vs recompute dW: {chk}")
+    assert chk.passed, chk
+    del dW_r
+    dh_s = rk.linear_logp_bwd_saved(h, W, tg, lse, g, saved)
+    assert torch.equal(dh_s.view(torch.int32), dh.view(torch.int32))
+    assert rk.get_device_error() == 0
