@@ -17,7 +17,8 @@ device time, inputs resident in HBM.  h (512 MB) and W (1.05 GB) exceed the
 126 MB L2, so nothing carries over between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-    python bench.py --case {fwd,bwd,dw,full,saved,logits,logits_bwd} [--shape T,H,V] [--reps R]
+    python bench.py --case {fwd,bwd,dw,full,saved,full_saved,logits,logits_bwd} [--shape T,H,V]
+                        [--reps R]
 
 `--case` runs one operator a few times on a small workload (for profiler
 captures; default T=2048, H=4096, V=32000: W and the logits exceed L2) and
@@ -60,9 +61,9 @@ WORKLOAD = ("grpo_fwd_bwd: linear_logp fwd+bwd T=65536 (64x1024) H=4096 V=128256
 # launch), recorded with the SHA-1 of the kernel source; reported only while the
 # source still matches.
 TRAFFIC_RECORD = {
-    "source_sha1": "5e28c9fe6022d190a72311ce936213c5df6f0f83",
-    "bytes_per_step": 138876524032,
-    "per_launch_gb": {"fwd_saved": 37.19, "dh": 101.68},
+    "source_sha1": "f289b4830e6ede3947760f76de84e52c4569af97",
+    "bytes_per_step": 161554138368,
+    "per_launch_gb": {"fwd_saved": 37.13, "dh": 124.42},
 }
 # Unique bytes a step has to move: forward h + W read, partials + target
 # logits + the softmax terms (T*V bf16) written; stash -> dZ pass: the terms
@@ -822,6 +823,18 @@ def run_case(args) -> None:
                 _, lse_s, _ = rk.linear_logp_fwd_saved(h, W, tg, saved=saved)
                 rk.linear_logp_bwd_saved(h, W, tg, lse_s, g, saved, dh=dh, workspace=wsb)
             flops = 4.0 * T * H * V
+        elif args.case == "full_saved":
+            # forward that keeps its softmax terms + dh and dW from them
+            saved = torch.empty(rk.linear_logp_saved_size(T, H, V), dtype=torch.uint8, device=dev)
+            ws = torch.empty(rk.linear_logp_bwd_full_workspace_size(T, H, V), dtype=torch.uint8,
+                             device=dev)
+            dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+            dh = torch.empty((T, H), dtype=torch.float32, device=dev)
+
+            def fn():
+                _, lse_s, _ = rk.linear_logp_fwd_saved(h, W, tg, saved=saved)
+                rk.linear_logp_bwd_full_saved(h, W, tg, lse_s, g, saved, dh=dh, dW=dW, workspace=ws)
+            flops = 6.0 * T * H * V
         elif args.case == "full":
             ws = torch.empty(rk.linear_logp_bwd_full_workspace_size(T, H, V), dtype=torch.uint8,
                              device=dev)
@@ -861,7 +874,8 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the separate timing of the widened rows")
-    ap.add_argument("--case", choices=["fwd", "bwd", "logits", "logits_bwd", "dw", "full", "saved"],
+    ap.add_argument("--case", choices=["fwd", "bwd", "logits", "logits_bwd", "dw", "full", "saved",
+                                       "full_saved"],
                     default=None)
     ap.add_argument("--shape", default="2048,4096,32000")
     ap.add_argument("--reps", type=int, default=3)

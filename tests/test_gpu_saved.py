@@ -222,3 +222,34 @@ def test_saved_full_backward_grpo(rk):
     dh_s = rk.linear_logp_bwd_saved(h, W, tg, lse, g, saved)
     assert torch.equal(dh_s.view(torch.int32), dh.view(torch.int32))
     assert rk.get_device_error() == 0
+
+
+@pytest.mark.slow
+def test_saved_path_llama_t1_t2_t3(rk):
+    # the Llama-shaped batch (T = 8192 varlen, H = 4096, V = 128256): logp,
+    # lse and dh of the picked sequences bitwise under T1 (a sequence alone),
+    # T2 (sequences reversed behind 77 pad rows) and T3 (neighbours redrawn)
+    pool = synth.llama_pool(with_grad=True)
+    W = cuda(pool.W)
+    n = len(pool.lengths)
+
+    def run(p, seqs, lead_pad=0):
+        lay = synth.packed(p, seqs, lead_pad=lead_pad)
+        h, tg, cu, g = cuda(lay.h), cuda(lay.targets), cuda(lay.cu_seqlens), cuda(lay.g)
+        logp, lse, dh = _saved_fwd_bwd(rk, h, W, tg, g, cu)
+        return lay, {"logp": logp.cpu(), "lse": lse.cpu(), "dh": dh.cpu()}
+
+    base_lay, base = run(pool, list(range(n)))
+    picks = [0, n // 2, n - 1]
+    variants = [(run(pool, [i]), [i]) for i in picks]
+    variants.append((run(pool, list(reversed(range(n))), lead_pad=77), picks))
+    other = synth.replace_neighbours(pool, picks, seed=2 + synth.NEIGHBOUR_SEED_OFFSET)
+    variants.append((run(other, list(range(n))), picks))
+    for (lay, out), seqs in variants:
+        for i in seqs:
+            b = torch.tensor(base_lay.rows_of[i])
+            v = torch.tensor(lay.rows_of[i])
+            for k in base:
+                assert torch.equal(out[k][v].view(torch.int32), base[k][b].view(torch.int32)), \
+                    (lay.description, i, k)
+    assert rk.get_device_error() == 0
