@@ -155,26 +155,46 @@ __global__ void __launch_bounds__(kConvThreads)
 }
 
 // dZ^T [V][ldn] from dZ [n][ldz] (bf16), through 64 x 64 tiles in shared
-// memory; token columns in [n, ldn) are written as 0.
+// memory; token columns in [n, ldn) are written as 0.  Global memory moves in
+// 16-byte vectors (8 bf16): ldz and ldn are multiples of 8.
 constexpr int kTrTile = 64;
+constexpr int kTrPitch = kTrTile;  // halfwords per shared row (16-byte aligned, swizzled groups)
 __global__ void __launch_bounds__(256)
     transpose_dz(const uint16_t *__restrict__ dz, int64_t ldz, int64_t n, int64_t V,
                  uint16_t *__restrict__ dzt, int64_t ldn) {
-    __shared__ uint16_t tile[kTrTile][kTrTile + 2];
-    const int tx = threadIdx.x % kTrTile, ty = threadIdx.x / kTrTile;  // 64 x 4
+    __shared__ __align__(16) uint16_t tile[kTrTile][kTrPitch];
     const int64_t t0 = (int64_t)blockIdx.x * kTrTile, v0 = (int64_t)blockIdx.y * kTrTile;
+    // load: 64 token rows x 8 vectors of 8 vocabulary columns, 2 per thread
 #pragma unroll
-    for (int j = 0; j < kTrTile / 4; ++j) {
-        const int r = ty + 4 * j;
-        const int64_t t = t0 + r, v = v0 + tx;
-        tile[r][tx] = (t < n && v < V) ? dz[t * ldz + v] : (uint16_t)0;
+    for (int j = 0; j < 2; ++j) {
+        const int idx = threadIdx.x + 256 * j;
+        const int r = idx >> 3, c8 = idx & 7;
+        const int64_t t = t0 + r, v = v0 + c8 * 8;
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (t < n && v < V) {
+            if (v + 8 <= ldz) {
+                x = *reinterpret_cast<const uint4 *>(dz + t * ldz + v);
+            }
+        }
+        // 8-column group g of row r sits at group g ^ (r / 8): the reads below
+        // (one column, 8 rows 8 apart) then fall in different banks
+        *reinterpret_cast<uint4 *>(&tile[r][((c8 ^ (r >> 3)) & 7) * 8]) = x;
     }
     __syncthreads();
+    // store: 64 vocabulary rows x 8 vectors of 8 tokens, 2 per thread
 #pragma unroll
-    for (int j = 0; j < kTrTile / 4; ++j) {
-        const int r = ty + 4 * j;
-        const int64_t v = v0 + r, t = t0 + tx;
-        if (v < V && t < ldn) dzt[v * ldn + t] = tile[tx][r];
+    for (int j = 0; j < 2; ++j) {
+        const int idx = threadIdx.x + 256 * j;
+        const int r = idx >> 3, c8 = idx & 7;  // r: vocabulary row in the tile
+        const int64_t v = v0 + r, t = t0 + c8 * 8;
+        if (v >= V || t >= ldn) continue;
+        // column r of rows c8 * 8 .. c8 * 8 + 7 (all with row / 8 == c8)
+        const int pc = ((((r >> 3) ^ c8) & 7) * 8) + (r & 7);
+        uint32_t q[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            q[k] = (uint32_t)tile[c8 * 8 + 2 * k][pc] | ((uint32_t)tile[c8 * 8 + 2 * k + 1][pc] << 16);
+        *reinterpret_cast<uint4 *>(dzt + v * ldn + t) = make_uint4(q[0], q[1], q[2], q[3]);
     }
 }
 

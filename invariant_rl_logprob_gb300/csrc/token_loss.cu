@@ -21,6 +21,11 @@ namespace {
 __global__ void __launch_bounds__(256)
     grpo_token_kernel(const float *__restrict__ logp, const int64_t *__restrict__ targets,
                       const int32_t *__restrict__ cu, int num_seqs, int64_t T, GrpoArgs p) {
+    // Launched with programmatic stream serialisation: the blocks may become
+    // resident while the previous kernel in the stream finishes, and wait here
+    // until it has completed and its writes (e.g. logp) are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T;
          t += (int64_t)gridDim.x * blockDim.x) {
         if (!row_active(t, targets[t], cu, num_seqs))
@@ -42,8 +47,16 @@ cudaError_t launch_grpo_token(const float *logp, const float *logp_old, const fl
     const int64_t cap = (int64_t)di.sm_count * 8;
     if (blocks > cap) blocks = cap;
     const GrpoArgs p{logp_old, logp_ref, adv, eps_low, eps_high, beta, scale, loss, grad, ratio, kl};
-    grpo_token_kernel<<<(unsigned)blocks, 256, 0, st>>>(logp, targets, cu, num_seqs, T, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, grpo_token_kernel, logp, targets, cu, num_seqs, T, p);
 }
 
 }  // namespace rk
