@@ -45,7 +45,7 @@
  *    failures return RK_ERR_CUDA (the CUDA error is left for
  *    cudaGetLastError / rk_last_cuda_error).
  *  - Thread safety: entry points may be called from several host threads.
- *    Shared state: the driver's tensor-map encoder, looked up once; per
+ *    Shared state: the CUDA driver's tensor-map encoder, looked up once; per
  *    device, the SM count and the device addresses of the library's static
  *    device variables (the error word, rk_linear_logp_noalloc's array), looked
  *    up on the first call on that device; the rk_set_row_blocks setting.

@@ -36,7 +36,7 @@ cudaError_t current_device_info(DeviceInfo *di);
 
 // Encodes a 2-D bf16 TMA descriptor over a row-major [outer, inner] matrix
 // with the given row stride (bytes) and box; 128-byte swizzle when `sw128`.
-// Returns false if the driver rejects it.
+// Returns false if the CUDA driver rejects it.
 bool encode_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                          bool sw128);

@@ -47,6 +47,8 @@ def test_host_only_calls(lib):
     assert lib.rk_status_string(3) == b"RK_ERR_WORKSPACE"
     lib.rk_version.restype = ctypes.c_char_p
     assert b"sm_103a" in lib.rk_version()
+    lib.rk_linear_logp_workspace_size.restype = ctypes.c_size_t
+    lib.rk_linear_logp_workspace_size.argtypes = [ctypes.c_int64] * 3
     f = lib.rk_linear_logp_workspace_size
     f.restype = ctypes.c_size_t
     f.argtypes = [ctypes.c_int64] * 3
@@ -121,6 +123,36 @@ def test_argument_errors_of_the_widened_rows(lib):
     st.restype = ctypes.c_int
     st.argtypes = [i64, vp]
     assert st(0, None) == 1 and st(20_000_000_000, None) == 1
+    # the forward that keeps its softmax terms and the backwards from them:
+    # argument errors found on the host
+    ss = lib.rk_linear_logp_saved_size
+    ss.restype, ss.argtypes = sz, [i64, i64, i64]
+    # the forward workspace, then the terms: round_up(V, 8) bf16 per row
+    assert ss(100, 64, 1001) == lib.rk_linear_logp_workspace_size(100, 64, 1001) + \
+        ((100 * 1008 * 2 + 255) // 256) * 256
+    assert ss(0, 64, 1001) == 0
+    fs = lib.rk_linear_logp_fwd_saved
+    fs.restype = ctypes.c_int
+    fs.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, sz, vp]
+    assert fs(fake, fake, fake, None, 0, 8, 64, 100, fake, None, None, 0, None) == 3   # no state
+    assert fs(fake, fake, fake, None, 0, 8, 64, 100, fake, None, ctypes.c_void_p(4096 + 16),
+              1 << 30, None) == 1                                               # misaligned
+    bs = lib.rk_linear_logp_bwd_saved
+    bs.restype = ctypes.c_int
+    bs.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, sz, vp, vp, sz, vp]
+    assert bs(fake, fake, fake, None, 0, 8, 96, 100, fake, fake, fake, 1 << 30, fake, fake,
+              1 << 30, None) == 2                                               # H % 64 != 0
+    assert bs(fake, fake, fake, None, 0, 8, 64, 100, fake, fake, fake, 16, fake, fake,
+              1 << 30, None) == 3                                               # state too small
+    bws = lib.rk_linear_logp_bwd_saved_workspace_size
+    bws.restype, bws.argtypes = sz, [i64, i64, i64]
+    assert bws(100, 64, 1001) == 256 + 512 + ((100 * 65 * 8 + 255) // 256) * 256
+    gp = lib.rk_linear_logp_grpo
+    gp.restype = ctypes.c_int
+    gp.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, f32, f32, f32, f32] + [vp] * 6 + \
+        [vp, sz, vp]
+    assert gp(fake, fake, fake, None, 0, 8, 64, 100, fake, None, fake, 1.5, 0.2, 0.0, 1.0,
+              fake, None, fake, fake, None, None, fake, 1 << 30, None) == 1     # eps_low >= 1
     # the dh / dW GEMM form: host-side setting and query only
     sr, lr = lib.rk_set_row_blocks, lib.rk_last_row_blocks
     sr.restype, sr.argtypes = ctypes.c_int, [i32]

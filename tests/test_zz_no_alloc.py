@@ -81,7 +81,7 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
 
 def test_noalloc_allocates_no_device_memory(lib):
     # After one warm-up call (which looks up the array's address and loads
-    # the kernels), further calls of other shapes leave both the driver's
+    # the kernels), further calls of other shapes leave both the CUDA driver's
     # free-memory count and PyTorch's allocator exactly where they were.
     h, W, tg, cu = workload(2048, 256, 50000, seed=93, varlen=True)
     h2, W2, tg2, _ = workload(700, 512, 9000, seed=94)
