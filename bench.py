@@ -521,9 +521,9 @@ def run_gpu(args) -> None:
     saved = torch.empty(rk.linear_logp_saved_size(T, H, V), dtype=torch.uint8, device=dev)
     ws_bwd = torch.empty(rk.linear_logp_bwd_saved_workspace_size(T, H, V), dtype=torch.uint8,
                          device=dev)
-    # fwd: tile kernel + merge; bwd: stash -> dZ, exact entries, entry sort,
-    # dh tile kernel, bad-target rows; logits: 1
-    launches_per_step = 2 + 5 + 1
+    # fwd: live row blocks, tile kernel, merge; bwd: stash -> dZ, exact
+    # entries, entry sort, dh tile kernel, bad-target / skipped rows; logits: 1
+    launches_per_step = 3 + 5 + 1
 
     def fwd(hh, tt, lp, ls):
         rk.linear_logp_fwd_saved(hh, W, tt, out=lp, lse=ls, saved=saved, stream=stream)

@@ -82,9 +82,11 @@ typedef enum {
 /*
  * Bytes of workspace rk_linear_logp needs for T rows (>= 0).  The layout is
  * private: per-row, per-vocab-tile (max, sum-exp) partials, the target logit
- * of every row and the counter from which the tile kernel's CTA pairs take
- * their tiles.  Returns 0 if T == 0.  Calls running at the same time need
- * separate workspaces.
+ * of every row, a flag per block of 256 rows telling whether it holds an
+ * active row (blocks without one get no tensor work: padding is free), and
+ * the counter from which the tile kernel's CTA pairs take their tiles.
+ * Returns 0 if T == 0.  Calls running at the same time need separate
+ * workspaces.
  */
 size_t rk_linear_logp_workspace_size(int64_t T, int64_t H, int64_t V);
 

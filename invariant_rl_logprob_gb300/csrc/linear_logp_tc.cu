@@ -81,6 +81,7 @@ constexpr int kMmaWarp = 5;
 constexpr int kThreads = kEpiThreads + 64;
 constexpr int kGroupN = 16;  // raster group (in N tiles) of the forward / dZ GEMMs
 constexpr int kGroupNDh = 8;  // raster group (in H tiles) of the dh and dW GEMMs
+static_assert(2 * BM == kLiveBlockRows, "a live flag covers one pair tile of rows");
 
 // kFwd: forward partials; kDz: backward GEMM 1; kDh: backward GEMM 2;
 // kLogits: the dense path's lm_head (z stored as bf16); kGreedy: kFwd plus
@@ -170,6 +171,10 @@ struct TileArgs {
     int64_t ntok;            // kDzT: number of canonical token positions (columns)
     // tile counter (zeroed before the launch); null: static round-robin order
     unsigned *tile_counter;
+    // per 256-row block of the launch: 0 when none of its rows is active, and
+    // its tiles are then never handed out (their rows' outputs are written
+    // elsewhere); null: every block is computed
+    const uint8_t *live;
     // kDz
     const float *lse;   // [T] (global)
     const float *grad;  // [T] (global)
@@ -239,6 +244,20 @@ __device__ __forceinline__ void tile_coords(int64_t tile, const TileArgs &a, int
         mb = (int)(r / gn);
         nb = n0 + (int)(r % gn);
     }
+}
+
+// Whether a tile holds an active row (any of its TileCfg::kMB row blocks).
+template <int MODE>
+__device__ __forceinline__ bool tile_live(int64_t tile, const TileArgs &a) {
+    if (a.live == nullptr) return true;
+    int mb, nb;
+    tile_coords<MODE>(tile, a, mb, nb);
+#pragma unroll
+    for (int j = 0; j < TileCfg<MODE>::kMB; ++j) {
+        const int64_t b = (int64_t)mb * TileCfg<MODE>::kMB + j;
+        if (b < a.num_m && a.live[b] != 0) return true;
+    }
+    return false;
 }
 
 template <int MODE>
@@ -330,12 +349,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    // the next tile that holds an active row
                     int64_t t;
-                    if (a.tile_counter) {
-                        t = (int64_t)atomicAdd(a.tile_counter, 1u);
-                    } else {
-                        t = next_static;
-                        next_static += npairs;
+                    for (;;) {
+                        if (a.tile_counter) {
+                            t = (int64_t)atomicAdd(a.tile_counter, 1u);
+                        } else {
+                            t = next_static;
+                            next_static += npairs;
+                        }
+                        if (t >= total || tile_live<MODE>(t, a)) break;
                     }
                     tv = t < total ? (int32_t)t : -1;
                     for (uint32_t r = 0; r < 2; ++r) {
@@ -1055,14 +1078,29 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
 // Backward rows with a target >= V get NaN gradients (and the error bit).
 __global__ void linear_logp_bwd_badtarget(const int64_t *__restrict__ targets,
                                           const int32_t *__restrict__ cu, int num_seqs, int64_t T,
-                                          int32_t V, int32_t H, float *__restrict__ dh,
-                                          unsigned *err) {
+                                          int32_t V, int32_t H, const uint8_t *__restrict__ live,
+                                          float *__restrict__ dh, unsigned *err) {
     const int64_t row = blockIdx.x;
     if (row >= T) return;
+    if (live != nullptr && live[row / kLiveBlockRows] == 0) {  // a block the dh GEMM skipped
+        for (int k = threadIdx.x; k < H; k += blockDim.x) dh[row * H + k] = 0.f;
+        return;
+    }
     const int64_t tgt = targets[row];
     if (!row_active(row, tgt, cu, num_seqs) || tgt < V) return;
     for (int k = threadIdx.x; k < H; k += blockDim.x) dh[row * H + k] = __int_as_float(0x7fc00000);
     if (threadIdx.x == 0) atomicOr(err, kErrTargetRange);
+}
+
+// live[b] = whether any of rows [row0 + 256 b, row0 + 256 b + 256) is active.
+__global__ void __launch_bounds__(2 * BM)
+    row_blocks_live(const int64_t *__restrict__ targets, const int32_t *__restrict__ cu,
+                    int num_seqs, int64_t row0, int64_t rows, uint8_t *__restrict__ live) {
+    const int64_t r = (int64_t)blockIdx.x * (2 * BM) + threadIdx.x;
+    bool act = false;
+    if (r < rows) act = row_active(row0 + r, targets[row0 + r], cu, num_seqs);
+    const int any = __syncthreads_or(act ? 1 : 0);
+    if (threadIdx.x == 0) live[blockIdx.x] = any != 0 ? 1 : 0;
 }
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -1154,12 +1192,31 @@ int last_row_blocks(RowGemm which) { return g_last_row_blocks[(int)which]; }
 // launches in one 256-byte slot of it.
 constexpr size_t kCounterBytes = 256;
 
+// Forward workspace: tile partials [T][num_n], target logits [T], the
+// row blocks' live flags [ceil(T / 256)], the tile counter.
 size_t linear_fwd_workspace_bytes(int64_t T, int64_t V) {
     if (T <= 0) return 0;
     const int64_t num_n = (V + BN - 1) / BN;
     return round256((size_t)T * (size_t)num_n * sizeof(float2)) + round256((size_t)T * sizeof(float)) +
-           kCounterBytes;
+           round256((size_t)((T + 2 * BM - 1) / (2 * BM))) + kCounterBytes;
 }
+
+namespace {
+uint8_t *fwd_live_flags(void *workspace, int64_t T, int64_t V) {
+    return reinterpret_cast<uint8_t *>(workspace) + linear_fwd_workspace_bytes(T, V) - kCounterBytes -
+           round256((size_t)((T + 2 * BM - 1) / (2 * BM)));
+}
+
+// Flags the row blocks of [0, T) that hold an active row (the forward's tile
+// kernel then skips the others: a padded batch costs no tensor work for its
+// padding).
+cudaError_t mark_live_blocks(const int64_t *targets, const int32_t *cu, int num_seqs, int64_t T,
+                             uint8_t *live, cudaStream_t st) {
+    row_blocks_live<<<(unsigned)((T + 2 * BM - 1) / (2 * BM)), 2 * BM, 0, st>>>(targets, cu, num_seqs,
+                                                                             0, T, live);
+    return cudaGetLastError();
+}
+}  // namespace
 
 cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
                               const int32_t *cu, int num_seqs, int64_t T, int64_t H, int64_t V,
@@ -1189,7 +1246,11 @@ cudaError_t launch_linear_fwd(const uint16_t *h, const uint16_t *W, const int64_
                                        round256((size_t)T * (size_t)a.num_n * sizeof(float2)));
     a.tile_counter = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(workspace) +
                                                   linear_fwd_workspace_bytes(T, V) - kCounterBytes);
-    cudaError_t e = run_tiles<kFwd>(tmA, tmB, a, di, st);
+    uint8_t *live = fwd_live_flags(workspace, T, V);
+    a.live = live;
+    cudaError_t e = mark_live_blocks(targets, cu, num_seqs, T, live, st);
+    if (e != cudaSuccess) return e;
+    e = run_tiles<kFwd>(tmA, tmB, a, di, st);
     if (e != cudaSuccess) return e;
 
     const unsigned mgrid = (unsigned)((T + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock);
@@ -1241,7 +1302,11 @@ cudaError_t launch_linear_fwd_saved(const uint16_t *h, const uint16_t *W, const 
     a.part = reinterpret_cast<float2 *>(w);
     a.ztgt = reinterpret_cast<float *>(w + round256((size_t)T * (size_t)a.num_n * sizeof(float2)));
     a.tile_counter = reinterpret_cast<unsigned *>(w + fwd_bytes - kCounterBytes);
-    cudaError_t e = run_tiles<kFwdS>(tmA, tmB, a, di, st, nullptr, &tmS);
+    uint8_t *live = fwd_live_flags(saved, T, V);
+    a.live = live;
+    cudaError_t e = mark_live_blocks(targets, cu, num_seqs, T, live, st);
+    if (e != cudaSuccess) return e;
+    e = run_tiles<kFwdS>(tmA, tmB, a, di, st, nullptr, &tmS);
     if (e != cudaSuccess) return e;
     const unsigned mgrid = (unsigned)((T + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock);
     linear_logp_merge<false><<<mgrid, 32 * kMergeRowsPerBlock, 0, st>>>(
@@ -1266,6 +1331,9 @@ cudaError_t launch_linear_bwd_saved(const uint16_t *h, const uint16_t *W, const 
     uint8_t *sv = reinterpret_cast<uint8_t *>(saved);
     const float2 *part = reinterpret_cast<const float2 *>(sv);
     uint16_t *dz = reinterpret_cast<uint16_t *>(sv + linear_fwd_workspace_bytes(T, V));
+    // the forward's flags of the row blocks holding an active row: the others
+    // are neither converted nor multiplied, and get dh = 0 at the end
+    const uint8_t *live = fwd_live_flags(saved, T, V);
     uint8_t *w = reinterpret_cast<uint8_t *>(workspace);
     unsigned *counter = reinterpret_cast<unsigned *>(w);
     int32_t *ecount = reinterpret_cast<int32_t *>(w + kCounterBytes);
@@ -1295,6 +1363,7 @@ cudaError_t launch_linear_bwd_saved(const uint16_t *h, const uint16_t *W, const 
         a.dh = dh;
         a.ecount = ecount + r0;
         a.ent = ent + r0 * kEntCap;
+        a.live = live + r0 / kLiveBlockRows;  // r0 = 0
         a.num_m = (int32_t)((rows + 2 * BM - 1) / (2 * BM));
         a.num_n = (int32_t)((H + BN - 1) / BN);
         a.num_k = (int32_t)((V + BK - 1) / BK);
@@ -1305,7 +1374,7 @@ cudaError_t launch_linear_bwd_saved(const uint16_t *h, const uint16_t *W, const 
     // exact z and sorted by column
     auto convert = [&](int64_t r0, int64_t rows, cudaStream_t s) -> cudaError_t {
         cudaError_t e2 = launch_stash_to_dz(dz, ldz, part, num_n, targets, cu, num_seqs, r0, rows, V,
-                                            lse, grad, ecount, ent, di, s);
+                                            lse, grad, live, ecount, ent, di, s);
         if (e2 != cudaSuccess) return e2;
         e2 = launch_exact_entries(h, W, H, targets, cu, num_seqs, r0, rows, V, lse, grad, ecount,
                                   ent, s);
@@ -1320,8 +1389,9 @@ cudaError_t launch_linear_bwd_saved(const uint16_t *h, const uint16_t *W, const 
     if (e == cudaSuccess) e = convert(0, T, st);
     if (e == cudaSuccess) e = dh_gemm(0, T);
     if (e != cudaSuccess) return e;
+    // rows of the blocks the forward found without an active row: dh = 0
     linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(targets, cu, num_seqs, T, (int32_t)V,
-                                                          (int32_t)H, dh, di.err);
+                                                          (int32_t)H, live, dh, di.err);
     return cudaGetLastError();
 }
 
@@ -1447,8 +1517,8 @@ cudaError_t launch_linear_bwd_full(const uint16_t *h, const uint16_t *W, const i
                            workspace, di, st, saved);
     if (e != cudaSuccess) return e;
     if (T > 0) {
-        linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(targets, cu, num_seqs, T,
-                                                              (int32_t)V, (int32_t)H, dh, di.err);
+        linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(
+            targets, cu, num_seqs, T, (int32_t)V, (int32_t)H, nullptr, dh, di.err);
         e = cudaGetLastError();
     }
     return e;
@@ -1746,7 +1816,7 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
         if (e != cudaSuccess) return e;
     }
     linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(targets, cu, num_seqs, T, (int32_t)V,
-                                                          (int32_t)H, dh, di.err);
+                                                          (int32_t)H, nullptr, dh, di.err);
     return cudaGetLastError();
 }
 

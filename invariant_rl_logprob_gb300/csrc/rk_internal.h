@@ -90,6 +90,8 @@ cudaError_t launch_grpo_token(const float *logp, const float *logp_old, const fl
 // target).  The lists are filled in any order and then sorted by column, so
 // every later sum over them runs in one fixed order.
 constexpr int kEntCap = 65;
+// Rows per block of the live flags (one tile row of the CTA-pair kernel).
+constexpr int kLiveBlockRows = 256;
 constexpr float kEntTau = 1.0f / 64.0f;
 // Sorts each of the first `rows` lists by column (one warp per row).
 cudaError_t launch_sort_entries(int32_t *ecount, int2 *ent, int64_t rows, cudaStream_t st);
@@ -168,12 +170,14 @@ cudaError_t launch_linear_bwd_saved(const uint16_t *h, const uint16_t *W, const 
                                     int64_t V, const float *lse, const float *grad, void *saved,
                                     float *dh, void *workspace, const DeviceInfo &di,
                                     cudaStream_t st);
-// The elementwise steps over rows [row0, row0 + rows).
+// The elementwise steps over rows [row0, row0 + rows).  live (or null) flags
+// the kLiveBlockRows-row blocks, counted from row 0, that hold an active row;
+// the rows of other blocks are left untouched.
 cudaError_t launch_stash_to_dz(uint16_t *dz, int64_t ldz, const float2 *part, int32_t num_n,
                                const int64_t *targets, const int32_t *cu, int num_seqs,
                                int64_t row0, int64_t rows, int64_t V, const float *lse,
-                               const float *grad, int32_t *ecount, int2 *ent, const DeviceInfo &di,
-                               cudaStream_t st);
+                               const float *grad, const uint8_t *live, int32_t *ecount, int2 *ent,
+                               const DeviceInfo &di, cudaStream_t st);
 // Conversion into canonical order (the dW backward) and dZ -> dZ^T.
 cudaError_t launch_stash_to_dz_canonical(const uint16_t *terms, int64_t ldz, const float2 *part,
                                          int32_t num_n, const int64_t *crow,

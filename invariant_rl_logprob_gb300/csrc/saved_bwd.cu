@@ -98,9 +98,11 @@ __global__ void __launch_bounds__(kConvThreads)
     stash_to_dz(uint16_t *__restrict__ dz, int64_t ldz, const float2 *__restrict__ part,
                 int32_t num_n, const int64_t *__restrict__ targets, const int32_t *__restrict__ cu,
                 int num_seqs, int64_t row0, int64_t V, const float *__restrict__ lse,
-                const float *__restrict__ grad, int32_t *__restrict__ ecount,
-                int2 *__restrict__ ent, unsigned *err) {
+                const float *__restrict__ grad, const uint8_t *__restrict__ live,
+                int32_t *__restrict__ ecount, int2 *__restrict__ ent, unsigned *err) {
     const int64_t row = row0 + blockIdx.x;
+    // a row block without active rows is skipped by the dh GEMM too
+    if (live != nullptr && live[row / kLiveBlockRows] == 0) return;
     const int64_t tgt = targets[row];
     const bool active = row_active(row, tgt, cu, num_seqs) && tgt < V;
     uint16_t *drow = dz + row * ldz;
@@ -244,14 +246,14 @@ __global__ void __launch_bounds__(32 * kExactRowsPerBlock)
 cudaError_t launch_stash_to_dz(uint16_t *dz, int64_t ldz, const float2 *part, int32_t num_n,
                                const int64_t *targets, const int32_t *cu, int num_seqs,
                                int64_t row0, int64_t rows, int64_t V, const float *lse,
-                               const float *grad, int32_t *ecount, int2 *ent, const DeviceInfo &di,
-                               cudaStream_t st) {
+                               const float *grad, const uint8_t *live, int32_t *ecount, int2 *ent,
+                               const DeviceInfo &di, cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
     const int64_t segs = (V + kConvCols - 1) / kConvCols;
     if (segs > 65535) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)rows, (unsigned)segs);
     stash_to_dz<<<grid, kConvThreads, 0, st>>>(dz, ldz, part, num_n, targets, cu, num_seqs, row0, V,
-                                              lse, grad, ecount, ent, di.err);
+                                              lse, grad, live, ecount, ent, di.err);
     return cudaGetLastError();
 }
 

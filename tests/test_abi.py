@@ -52,9 +52,10 @@ def test_host_only_calls(lib):
     f = lib.rk_linear_logp_workspace_size
     f.restype = ctypes.c_size_t
     f.argtypes = [ctypes.c_int64] * 3
-    # T rows x ceil(V/256) tiles x 8 bytes + T x 4 bytes, each rounded to 256,
-    # + 256 bytes for the tile counter
-    assert f(8192, 4096, 128256) == 8192 * 501 * 8 + 8192 * 4 + 256
+    # T rows x ceil(V/256) tiles x 8 bytes + T x 4 bytes + one live flag per
+    # 256 rows, each rounded to 256, + 256 bytes for the tile counter
+    assert f(8192, 4096, 128256) == 8192 * 501 * 8 + 8192 * 4 + 256 + 256
+    assert f(100, 64, 1001) == 256 * ((100 * 4 * 8 + 255) // 256) + 512 + 256 + 256
     assert f(0, 4096, 128256) == 0
     g = lib.rk_linear_logp_bwd_workspace_size
     g.restype = ctypes.c_size_t

@@ -150,6 +150,61 @@ def test_saved_path_grpo_sampled_rows(rk):
     assert rk.get_device_error() == 0
 
 
+def _saved_terms(rk, saved, T, H, V):
+    """The saved state's bf16 terms as raw bytes [T, ld * 2] (after the forward workspace)."""
+    ws = rk.linear_logp_workspace_size(T, H, V)
+    ld = (V + 7) // 8 * 8
+    return saved[ws:ws + T * ld * 2].view(T, ld * 2)
+
+
+@pytest.mark.parametrize("all_pad", [False, True])
+def test_padding_blocks_are_skipped(rk, all_pad):
+    # Sequences right-padded to 1024 rows: a block of 256 rows holding no
+    # active row gets no tensor work.  Visible: the forward leaves the block's
+    # saved terms as the buffer held them, and the backward writes dh = 0 there
+    # over a NaN-filled output.  logp and lse are 0 there, and the active rows
+    # are the packed layout's bits.
+    H, V = 256, 3000
+    pool = synth.make_pool(H, V, [300, 40, 700, 129], seed=93, with_grad=True)
+    seqs = [0, 1, 2, 3]
+    lay = synth.padded(pool, seqs, 1024)
+    if all_pad:
+        lay.targets[:] = -100
+    T = lay.T
+    W = cuda(pool.W)
+
+    def run(l, sentinel):
+        h, tg, g = cuda(l.h), cuda(l.targets), cuda(l.g)
+        saved = torch.full((rk.linear_logp_saved_size(l.T, H, V),), sentinel, dtype=torch.uint8,
+                           device=DEV)
+        lp, lse, saved = rk.linear_logp_fwd_saved(h, W, tg, saved=saved)
+        terms = _saved_terms(rk, saved, l.T, H, V).clone()  # the backward rewrites them
+        dh = torch.full((l.T, H), float("nan"), device=DEV)
+        rk.linear_logp_bwd_saved(h, W, tg, lse, g, saved, dh=dh)
+        return lp.cpu(), lse.cpu(), dh.cpu(), terms.cpu()
+
+    lp, lse, dh, terms = run(lay, 0xAB)
+    dead = (lay.targets.view(-1, 256) < 0).all(dim=1)
+    assert int(dead.sum()) == (16 if all_pad else 9)
+    for b in range(T // 256):
+        rows = slice(256 * b, 256 * b + 256)
+        if dead[b]:
+            assert bool((terms[rows] == 0xAB).all()), f"block {b} was computed"
+        else:
+            assert not bool((terms[rows] == 0xAB).all())
+    inactive = lay.targets < 0
+    assert bool((lp[inactive] == 0).all()) and bool((lse[inactive] == 0).all())
+    assert bool((dh[inactive] == 0).all())
+    if not all_pad:
+        pk = synth.packed(pool, seqs)
+        lp_p, lse_p, dh_p, _ = run(pk, 0)
+        for i in seqs:
+            a, b = lay.rows_of[i], pk.rows_of[i]
+            assert same_bits(lp[a], lp_p[b]) and same_bits(lse[a], lse_p[b])
+            assert same_bits(dh[a], dh_p[b])
+    assert rk.get_device_error() == 0
+
+
 # --------------------------------------------------------------------------
 # dh and dW together from the saved terms (rk_linear_logp_bwd_full_saved)
 # --------------------------------------------------------------------------
