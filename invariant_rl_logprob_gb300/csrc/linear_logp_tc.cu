@@ -1077,12 +1077,14 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
 
 // Backward rows with a target >= V get NaN gradients (and the error bit).
 __global__ void linear_logp_bwd_badtarget(const int64_t *__restrict__ targets,
-                                          const int32_t *__restrict__ cu, int num_seqs, int64_t T,
-                                          int32_t V, int32_t H, const uint8_t *__restrict__ live,
+                                          const int32_t *__restrict__ cu, int num_seqs,
+                                          int64_t row0, int64_t rows, int32_t V, int32_t H,
+                                          const uint8_t *__restrict__ live,
                                           float *__restrict__ dh, unsigned *err) {
-    const int64_t row = blockIdx.x;
-    if (row >= T) return;
-    if (live != nullptr && live[row / kLiveBlockRows] == 0) {  // a block the dh GEMM skipped
+    if ((int64_t)blockIdx.x >= rows) return;
+    const int64_t row = row0 + blockIdx.x;
+    // live: flags of the blocks of rows [row0, row0 + rows), or null
+    if (live != nullptr && live[blockIdx.x / kLiveBlockRows] == 0) {  // a block the dh GEMM skipped
         for (int k = threadIdx.x; k < H; k += blockDim.x) dh[row * H + k] = 0.f;
         return;
     }
@@ -1390,7 +1392,7 @@ cudaError_t launch_linear_bwd_saved(const uint16_t *h, const uint16_t *W, const 
     if (e == cudaSuccess) e = dh_gemm(0, T);
     if (e != cudaSuccess) return e;
     // rows of the blocks the forward found without an active row: dh = 0
-    linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(targets, cu, num_seqs, T, (int32_t)V,
+    linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(targets, cu, num_seqs, 0, T, (int32_t)V,
                                                           (int32_t)H, live, dh, di.err);
     return cudaGetLastError();
 }
@@ -1518,7 +1520,7 @@ cudaError_t launch_linear_bwd_full(const uint16_t *h, const uint16_t *W, const i
     if (e != cudaSuccess) return e;
     if (T > 0) {
         linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(
-            targets, cu, num_seqs, T, (int32_t)V, (int32_t)H, nullptr, dh, di.err);
+            targets, cu, num_seqs, 0, T, (int32_t)V, (int32_t)H, nullptr, dh, di.err);
         e = cudaGetLastError();
     }
     return e;
@@ -1728,11 +1730,11 @@ static cudaError_t canonical_backward(const uint16_t *h, const uint16_t *W, cons
 int64_t linear_bwd_chunk_quantum() { return BM; }
 
 // Backward workspace for a chunk of rows: tile counter, the rows' entry
-// counts and entry lists, then dZ.
+// counts and entry lists, dZ, then the live flags of the chunk's row blocks.
 size_t linear_bwd_chunk_bytes(int64_t rows, int64_t V) {
     const size_t r = (size_t)rows;
     return kCounterBytes + round256(r * 4) + round256(r * (size_t)kEntCap * 8) +
-           round256(r * (size_t)ld_dz(V) * 2);
+           round256(r * (size_t)ld_dz(V) * 2) + round256((r + kLiveBlockRows - 1) / kLiveBlockRows);
 }
 
 cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_t *targets,
@@ -1754,6 +1756,7 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
     int2 *ent = reinterpret_cast<int2 *>(w + kCounterBytes + round256((size_t)chunk * 4));
     uint16_t *dz = reinterpret_cast<uint16_t *>(w + kCounterBytes + round256((size_t)chunk * 4) +
                                                 round256((size_t)chunk * (size_t)kEntCap * 8));
+    uint8_t *live = reinterpret_cast<uint8_t *>(dz) + round256((size_t)chunk * (size_t)ldz * 2);
 
     CUtensorMap tmW_k, tmW_mn;
     if (!encode_tmap_bf16_2d(&tmW_k, W, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, BK, BN / 2, true))
@@ -1790,6 +1793,9 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
         a.ecount = ecount;
         a.ent = ent;
         a.num_m = (int32_t)((rows + 2 * BM - 1) / (2 * BM));
+        // the chunk's row blocks without an active row: skipped by both GEMMs
+        a.live = live;
+        row_blocks_live<<<(unsigned)a.num_m, 2 * BM, 0, st>>>(targets, cu, num_seqs, r0, rows, live);
 
         // GEMM 1: z recomputed, dZ = g exp(z - lse) in bf16 (the target and
         // p >= 1/64 columns as fp32 entries instead), stored by TMA
@@ -1814,10 +1820,14 @@ cudaError_t launch_linear_bwd(const uint16_t *h, const uint16_t *W, const int64_
         a.num_k = (int32_t)((V + BK - 1) / BK);
         e = run_rows<kDh, kDh2>(tmDz, tmW_mn, a, di, st, RowGemm::kDhGemm);
         if (e != cudaSuccess) return e;
+        // out-of-range targets, and dh = 0 on the skipped blocks
+        linear_logp_bwd_badtarget<<<(unsigned)rows, 128, 0, st>>>(targets, cu, num_seqs, r0, rows,
+                                                                 (int32_t)V, (int32_t)H, live, dh,
+                                                                 di.err);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
-    linear_logp_bwd_badtarget<<<(unsigned)T, 128, 0, st>>>(targets, cu, num_seqs, T, (int32_t)V,
-                                                          (int32_t)H, nullptr, dh, di.err);
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 }  // namespace rk

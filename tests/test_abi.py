@@ -61,8 +61,9 @@ def test_host_only_calls(lib):
     g.restype = ctypes.c_size_t
     g.argtypes = [ctypes.c_int64] * 3
     # tile counter, then per 128-row chunk: entry counts, entry lists
-    # (65 slots of 8 bytes), dZ; each part rounded to 256 bytes
-    assert g(100, 64, 1001) == 256 + 512 + 128 * 65 * 8 + 128 * 1008 * 2
+    # (65 slots of 8 bytes), dZ, a live flag per 256 rows; each part rounded
+    # to 256 bytes
+    assert g(100, 64, 1001) == 256 + 512 + 128 * 65 * 8 + 128 * 1008 * 2 + 256
 
 
 def test_argument_errors_return_before_any_launch(lib):

@@ -205,6 +205,43 @@ def test_padding_blocks_are_skipped(rk, all_pad):
     assert rk.get_device_error() == 0
 
 
+def test_padding_blocks_are_skipped_recompute(rk):
+    # The same for the recompute backward (rk_linear_logp_bwd), one chunk:
+    # the dZ rows of blocks without an active row keep what the workspace
+    # held, their dh is 0 over a NaN-filled output, and the active rows are
+    # the packed layout's bits.
+    H, V = 256, 3000
+    pool = synth.make_pool(H, V, [300, 40, 700, 129], seed=94, with_grad=True)
+    seqs = [0, 1, 2, 3]
+    lay = synth.padded(pool, seqs, 1024)
+    W = cuda(pool.W)
+    ld = (V + 7) // 8 * 8
+    r256 = lambda x: (x + 255) // 256 * 256
+
+    def run(l):
+        h, tg, g = cuda(l.h), cuda(l.targets), cuda(l.g)
+        _, lse = rk.linear_logp(h, W, tg)
+        ws = torch.full((rk.linear_logp_bwd_workspace_size(l.T, H, V),), 0xAB, dtype=torch.uint8,
+                        device=DEV)
+        dh = torch.full((l.T, H), float("nan"), device=DEV)
+        rk.linear_logp_bwd(h, W, tg, lse, g, dh=dh, workspace=ws)
+        off = 256 + r256(l.T * 4) + r256(l.T * 65 * 8)
+        return dh.cpu(), ws[off:off + l.T * ld * 2].view(l.T, ld * 2).cpu()
+
+    dh, dz = run(lay)
+    dead = (lay.targets.view(-1, 256) < 0).all(dim=1)
+    assert int(dead.sum()) == 9
+    for b in range(lay.T // 256):
+        rows = slice(256 * b, 256 * b + 256)
+        assert bool((dz[rows] == 0xAB).all()) == bool(dead[b]), f"block {b}"
+    assert bool((dh[lay.targets < 0] == 0).all())
+    pk = synth.packed(pool, seqs)
+    dh_p, _ = run(pk)
+    for i in seqs:
+        assert same_bits(dh[lay.rows_of[i]], dh_p[pk.rows_of[i]])
+    assert rk.get_device_error() == 0
+
+
 # --------------------------------------------------------------------------
 # dh and dW together from the saved terms (rk_linear_logp_bwd_full_saved)
 # --------------------------------------------------------------------------
