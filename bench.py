@@ -61,9 +61,9 @@ WORKLOAD = ("grpo_fwd_bwd: linear_logp fwd+bwd T=65536 (64x1024) H=4096 V=128256
 # launch), recorded with the SHA-1 of the kernel source; reported only while the
 # source still matches.
 TRAFFIC_RECORD = {
-    "source_sha1": "f289b4830e6ede3947760f76de84e52c4569af97",
-    "bytes_per_step": 161554138368,
-    "per_launch_gb": {"fwd_saved": 37.13, "dh": 124.42},
+    "source_sha1": "1052ea9230cd078c785de4a7ac0e5f2fd41c9224",
+    "bytes_per_step": 171500861440,
+    "per_launch_gb": {"fwd_saved": 37.20, "dh": 134.30},
 }
 # Unique bytes a step has to move: forward h + W read, partials + target
 # logits + the softmax terms (T*V bf16) written; stash -> dZ pass: the terms
