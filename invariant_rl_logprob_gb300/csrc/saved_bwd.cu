@@ -108,17 +108,27 @@ __global__ void __launch_bounds__(kConvThreads)
     uint16_t *drow = dz + row * ldz;
     const float g = active ? grad[row] : 0.f;
     const float l = active ? lse[row] : 0.f;
+    // all of the thread's loads first, then the conversions (1.3 % faster
+    // than loading each group just before converting it)
+    uint4 w[kConvGroupsPerThread];
+#pragma unroll
+    for (int i = 0; i < kConvGroupsPerThread; ++i) {
+        const int64_t c0 = (int64_t)blockIdx.y * kConvCols + (int64_t)i * (kConvThreads * 8) +
+                           (int64_t)threadIdx.x * 8;
+        // ldz % 8 == 0: 16-byte aligned
+        if (active && c0 < V) w[i] = *reinterpret_cast<const uint4 *>(drow + c0);
+    }
 #pragma unroll
     for (int i = 0; i < kConvGroupsPerThread; ++i) {
         const int64_t c0 = (int64_t)blockIdx.y * kConvCols + (int64_t)i * (kConvThreads * 8) +
                            (int64_t)threadIdx.x * 8;
         if (c0 >= V) continue;
-        uint4 *gp = reinterpret_cast<uint4 *>(drow + c0);  // ldz % 8 == 0: 16-byte aligned
+        uint4 *gp = reinterpret_cast<uint4 *>(drow + c0);
         if (!active) {
             *gp = make_uint4(0, 0, 0, 0);
             continue;
         }
-        *gp = convert_group(*gp, c0, V, tgt, part[row * num_n + c0 / kTileCols].x, l, g,
+        *gp = convert_group(w[i], c0, V, tgt, part[row * num_n + c0 / kTileCols].x, l, g,
                             ecount + row, ent + row * kEntCap, err);
     }
 }
