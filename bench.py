@@ -345,6 +345,7 @@ def measure_rows(rk, pool, zs, peaks, dev, stream) -> dict:
                               "unit": "GB/s", "peak": peaks["hbm_gbs"],
                               "frac": gbs / peaks["hbm_gbs"], "bytes_per_call": nbytes,
                               "note": "2.6 MB per call: launch-latency bound"}
+    out["decode_greedy_T64"] = measure_decode(rk, h[:64].clone(), W, dev)
     # fused greedy step on the whole group
     wsg = torch.empty(rk.linear_greedy_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
     ms = time_loop(lambda i: rk.linear_greedy(h, W, workspace=wsg, stream=stream), 3, stream)
@@ -437,6 +438,59 @@ def measure_rows(rk, pool, zs, peaks, dev, stream) -> dict:
     del wsf, wsb, dh
     out.update(measure_config_rows(rk, peaks, dev, stream))
     return out
+
+
+def measure_decode(rk, h, W, dev) -> dict:
+    """A greedy decode step (one new token for each of 64 sequences), as a
+    serving loop runs it: each step synchronised.  The same call eager and
+    captured once in a CUDA graph and replayed; both give the same bits."""
+    import torch
+    T, H, V = h.shape[0], h.shape[1], W.shape[0]
+    cs = torch.cuda.Stream(dev)
+    ws = torch.empty(rk.linear_greedy_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
+    cs.wait_stream(torch.cuda.current_stream(dev))
+
+    def greedy():
+        return rk.linear_greedy(h, W, workspace=ws, stream=cs)
+    for _ in range(5):
+        ref = greedy()
+    cs.synchronize()
+    n = 200
+    t0 = time.perf_counter()
+    for _ in range(n):
+        greedy()
+        cs.synchronize()
+    eager_us = (time.perf_counter() - t0) / n * 1e6
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cs):
+        cap = greedy()
+    with torch.cuda.stream(cs):
+        for _ in range(5):
+            graph.replay()
+    cs.synchronize()
+    same = bool(torch.equal(cap[0], ref[0]) and torch.equal(cap[1].view(torch.int32),
+                                                             ref[1].view(torch.int32)))
+    t0 = time.perf_counter()
+    with torch.cuda.stream(cs):
+        for _ in range(n):
+            graph.replay()
+            cs.synchronize()
+    graph_us = (time.perf_counter() - t0) / n * 1e6
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(cs):
+        a.record(cs)
+        for _ in range(n):
+            graph.replay()
+        b.record(cs)
+    b.synchronize()
+    dev_us = a.elapsed_time(b) / n * 1e3
+    del graph
+    return {"shape": [T, H, V], "eager_us_per_step": eager_us, "graph_us_per_step": graph_us,
+            "device_us_per_step": dev_us, "graph_bits_equal_eager": same,
+            "timing": "host wall clock per step, each step synchronised (eager: the Python "
+                      "binding's call; graph: one replay); device: back-to-back replays, "
+                      "CUDA events"}
 
 
 def measure_config_rows(rk, peaks, dev, stream) -> dict:
