@@ -455,6 +455,22 @@ rk_status rk_selftest_wait_timeout(int64_t limit_ns, void *stream);
 rk_status rk_set_row_blocks(int32_t n);
 int32_t rk_last_row_blocks(int32_t gemm);
 
+/*
+ * Tile order of the same GEMMs.  Long K loops (>= 256 stages) take their
+ * tiles in rounds: with P resident CTA pairs, pair p computes tiles p, p + P,
+ * ... and starts round r only once every pair has issued the copies of round
+ * r - 1, so the pairs that share a dZ row block or a W slice stay in step and
+ * share it through L2 (the dh GEMM's DRAM reads at T = 65536, V = 128256 fell
+ * from 115 to 84 GB).  That launch is cooperative (all pairs resident); if it
+ * is refused, or the stream is being captured into a graph, the tiles are
+ * taken from a counter in the order the pairs become free.  The order never
+ * changes a bit.
+ * rk_last_tile_order(gemm): 2 rounds, 1 counter, for the last such GEMM on
+ * the calling host thread (gemm 0 = dh, 1 = dW); 0 before the first launch,
+ * -1 for another gemm value.
+ */
+int32_t rk_last_tile_order(int32_t gemm);
+
 /* Human-readable name of a status code (static string). */
 const char *rk_status_string(rk_status s);
 

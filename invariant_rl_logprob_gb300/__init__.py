@@ -137,6 +137,8 @@ def load_library() -> ctypes.CDLL:
     lib.rk_set_row_blocks.restype = ctypes.c_int
     lib.rk_last_row_blocks.argtypes = [i32]
     lib.rk_last_row_blocks.restype = i32
+    lib.rk_last_tile_order.argtypes = [i32]
+    lib.rk_last_tile_order.restype = i32
     _lib = lib
     return lib
 
@@ -608,6 +610,13 @@ def last_row_blocks(gemm: str) -> int:
     """Row blocks per tile of the last ``"dh"`` or ``"dw"`` GEMM launched on
     this thread (0 before the first)."""
     return int(load_library().rk_last_row_blocks({"dh": 0, "dw": 1}[gemm]))
+
+
+def last_tile_order(gemm: str) -> int:
+    """Tile order of the last ``"dh"`` or ``"dw"`` GEMM launched on this
+    thread: 2 rounds started together, 1 tiles from a counter, 0 before the
+    first."""
+    return int(load_library().rk_last_tile_order({"dh": 0, "dw": 1}[gemm]))
 
 
 def get_device_error(stream: torch.cuda.Stream | None = None) -> int:

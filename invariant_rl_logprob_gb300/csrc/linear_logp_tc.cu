@@ -175,6 +175,13 @@ struct TileArgs {
     // its tiles are then never handed out (their rows' outputs are written
     // elsewhere); null: every block is computed
     const uint8_t *live;
+    // Rounds (non-null; tile_counter is then null): pair p takes tiles p,
+    // p + P, p + 2P, ... (P pairs), and starts the tiles of round r only when
+    // every pair has issued all copies of round r - 1 (each pair adds one to
+    // this counter per round).  The tiles of a round then run in step and
+    // share their dZ row blocks and W slices through L2.  Launched
+    // cooperatively, so that every pair is resident.
+    unsigned *wave_ctr;
     // kDz
     const float *lse;   // [T] (global)
     const float *grad;  // [T] (global)
@@ -244,6 +251,31 @@ __device__ __forceinline__ void tile_coords(int64_t tile, const TileArgs &a, int
         mb = (int)(r / gn);
         nb = n0 + (int)(r % gn);
     }
+}
+
+// Rounds of tiles (TileArgs::wave_ctr).  Before tile t (round t / npairs),
+// the pair signals every round up to that one and waits until all npairs
+// pairs have signalled it; a pair with no more tiles (t >= total) signals all
+// remaining rounds and returns.  Bounded: after kWaitLimitNs the pair raises
+// the abort flag and RK_DEVERR_TIMEOUT, signals the remaining rounds (so the
+// others are not held) and returns false.
+__device__ __noinline__ bool wait_round(unsigned *ctr, int64_t t, int64_t total, int64_t npairs,
+                                        int64_t &arrived, volatile int *abort, unsigned *err) {
+    const int64_t rounds = (total + npairs - 1) / npairs;
+    const int64_t rnd = t < total ? t / npairs : rounds - 1;
+    for (; arrived < rnd; ++arrived) atomicAdd(ctr, 1u);
+    if (t >= total) return true;
+    const unsigned need = (unsigned)(npairs * rnd);
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 0; *reinterpret_cast<volatile unsigned *>(ctr) < need; ++i) {
+        if ((i & 63u) == 0 && (*abort || global_timer_ns() - t0 > kWaitLimitNs)) {
+            *abort = 1;
+            atomicOr(err, kErrTimeout);
+            for (; arrived < rounds - 1; ++arrived) atomicAdd(ctr, 1u);
+            return false;
+        }
+    }
+    return true;
 }
 
 // Whether a tile holds an active row (any of its TileCfg::kMB row blocks).
@@ -341,6 +373,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int q = 0;
             uint32_t qph = 0;
             int64_t next_static = pair;
+            int64_t rounds_arrived = 0;  // wave_ctr: rounds this pair has signalled
             while (ok) {
                 int32_t tv;
                 if (rank == 0) {
@@ -360,6 +393,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                         if (t >= total || tile_live<MODE>(t, a)) break;
                     }
+                    if (a.wave_ctr != nullptr && !wait_round(a.wave_ctr, t, total, npairs,
+                                                             rounds_arrived, abort, a.err))
+                        t = total;  // gave up: no more tiles for this pair
                     tv = t < total ? (int32_t)t : -1;
                     for (uint32_t r = 0; r < 2; ++r) {
                         st_shared_cluster_u32(mapa_shared(smem_u32(&ctl->tq[q]), r), (uint32_t)tv);
@@ -420,6 +456,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ph ^= 1u;
                     }
                 }
+            }
+            if (rank == 0 && a.wave_ctr != nullptr) {
+                // every round signalled, however the loop ended, so that no
+                // other pair waits for this one
+                const int64_t rounds = (total + npairs - 1) / npairs;
+                for (; rounds_arrived < rounds - 1; ++rounds_arrived) atomicAdd(a.wave_ctr, 1u);
             }
             if (!ok) {  // let every issued copy land before the pair exits
                 if (rank == 0) {
@@ -1149,12 +1191,29 @@ cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tile
     if (tiles == 0) return cudaSuccess;
     const int64_t pairs = std::min<int64_t>(tiles, resident_pairs<MODE>(di));
     const unsigned grid = (unsigned)(2 * pairs);
+    CUtensorMap unused;
+    std::memset(&unused, 0, sizeof(unused));
+    if (a.wave_ctr) {
+        // rounds: every pair must be resident, so the launch is cooperative
+        e = cudaMemsetAsync(a.wave_ctr, 0, sizeof(unsigned), st);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = TileCfg<MODE>::kSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, linear_logp_tiles<MODE>, tmA, tmB, tmC ? *tmC : unused,
+                                  tmD ? *tmD : unused, a);
+    }
     if (a.tile_counter) {
         e = cudaMemsetAsync(a.tile_counter, 0, sizeof(unsigned), st);
         if (e != cudaSuccess) return e;
     }
-    CUtensorMap unused;
-    std::memset(&unused, 0, sizeof(unused));
     linear_logp_tiles<MODE><<<grid, kThreads, TileCfg<MODE>::kSmem, st>>>(
         tmA, tmB, tmC ? *tmC : unused, tmD ? *tmD : unused, a);
     return cudaGetLastError();
@@ -1169,6 +1228,8 @@ cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tile
 // form each GEMM last used on this host thread is kept for rk_last_row_blocks.
 std::atomic<int> g_row_blocks_override{0};
 thread_local int g_last_row_blocks[2] = {0, 0};
+// Tile order of the last dh / dW GEMM on this host thread: 1 counter, 2 rounds.
+thread_local int g_last_tile_order[2] = {0, 0};
 
 template <int M1, int M2>
 cudaError_t run_rows(const CUtensorMap &tmA, const CUtensorMap &tmB, const TileArgs &a,
@@ -1178,6 +1239,32 @@ cudaError_t run_rows(const CUtensorMap &tmA, const CUtensorMap &tmB, const TileA
     const bool use_two =
         force == 2 || (force == 0 && a.num_k >= 256 && two >= 8 * resident_pairs<M2>(di));
     g_last_row_blocks[(int)which] = use_two ? 2 : 1;
+    // Long K loops take their tiles in rounds (TileArgs::wave_ctr): pairs
+    // that share a dZ row block or a W slice then stay in step, which cut the
+    // dh GEMM's DRAM reads at the GRPO size from 115 to 84 GB.  The round
+    // counter sits 64 bytes into the launch's 256-byte counter slot.  If the
+    // cooperative launch is refused, the tiles come from the counter instead
+    // (the order never changes a bit).
+    // (Not while the stream is being captured into a graph: there the tiles
+    // come from the counter.)
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &capturing) != cudaSuccess) {
+        (void)cudaGetLastError();
+        capturing = cudaStreamCaptureStatusActive;
+    }
+    if (a.tile_counter != nullptr && a.num_k >= 256 && capturing == cudaStreamCaptureStatusNone) {
+        TileArgs w = a;
+        w.wave_ctr = a.tile_counter + 16;
+        w.tile_counter = nullptr;
+        const cudaError_t e = use_two ? run_tiles<M2>(tmA, tmB, w, di, st)
+                                      : run_tiles<M1>(tmA, tmB, w, di, st);
+        if (e == cudaSuccess) {
+            g_last_tile_order[(int)which] = 2;
+            return e;
+        }
+        (void)cudaGetLastError();
+    }
+    g_last_tile_order[(int)which] = 1;
     if (use_two) return run_tiles<M2>(tmA, tmB, a, di, st);
     return run_tiles<M1>(tmA, tmB, a, di, st);
 }
@@ -1189,6 +1276,7 @@ int64_t ld_dzt(int64_t n) { return ld_dz(n); }         // dZ^T rows (tokens)
 
 void set_row_blocks_override(int n) { g_row_blocks_override.store(n, std::memory_order_relaxed); }
 int last_row_blocks(RowGemm which) { return g_last_row_blocks[(int)which]; }
+int last_tile_order(RowGemm which) { return g_last_tile_order[(int)which]; }
 
 // Every launcher with a workspace keeps the tile counter of its tile
 // launches in one 256-byte slot of it.

@@ -502,6 +502,11 @@ int32_t rk_last_row_blocks(int32_t gemm) {
     return (int32_t)rk::last_row_blocks(gemm == 0 ? rk::RowGemm::kDhGemm : rk::RowGemm::kDwGemm);
 }
 
+int32_t rk_last_tile_order(int32_t gemm) {
+    if (gemm != 0 && gemm != 1) return -1;
+    return (int32_t)rk::last_tile_order(gemm == 0 ? rk::RowGemm::kDhGemm : rk::RowGemm::kDwGemm);
+}
+
 rk_status rk_linear_logp_bwd_full_saved(const uint16_t *h, const uint16_t *W,
                                         const int64_t *targets, const int32_t *cu_seqlens,
                                         int32_t num_seqs, int64_t T, int64_t H, int64_t V,

@@ -156,6 +156,9 @@ enum class RowGemm { kDhGemm = 0, kDwGemm = 1 };
 void set_row_blocks_override(int n);
 // Blocks per tile of the last dh / dW GEMM launched on this host thread (0: none yet).
 int last_row_blocks(RowGemm which);
+// Tile order of the last dh / dW GEMM launched on this host thread: 1 tiles
+// from a counter, 2 rounds started together (0: none yet).
+int last_tile_order(RowGemm which);
 
 // ---- forward that saves its exponentials; backward from them ----
 // (linear_logp_tc.cu; the elementwise steps in saved_bwd.cu)

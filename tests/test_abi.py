@@ -162,3 +162,6 @@ def test_argument_errors_of_the_widened_rows(lib):
     assert sr(3) == 1 and sr(-1) == 1
     assert sr(2) == 0 and sr(1) == 0 and sr(0) == 0
     assert lr(0) == 0 and lr(1) == 0 and lr(2) == -1    # no GEMM launched in this thread
+    lt = lib.rk_last_tile_order
+    lt.restype, lt.argtypes = i32, [i32]
+    assert lt(0) == 0 and lt(1) == 0 and lt(-1) == -1

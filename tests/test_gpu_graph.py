@@ -103,3 +103,35 @@ def test_greedy_decode_graph_replays_eager_bits(rk):
         assert torch.equal(out["tok"], tok)
         assert same_bits(out["logp"], lp) and same_bits(out["lse"], ls)
     assert rk.get_device_error() == 0
+
+
+@pytest.mark.parametrize("blocks", [1, 2])
+def test_rounds_and_counter_tile_orders_agree(rk, blocks):
+    # V = 16384: the dh GEMM's K loop has 256 stages, so an eager call takes
+    # its tiles in rounds (a cooperative launch; 128 one-block tiles are two
+    # rounds of the resident pairs); inside a graph capture the same GEMM
+    # takes them from the counter.  Same bits, in either tile form.
+    H, V = 2048, 16384
+    pool = synth.make_pool(H, V, [1500, 1000, 1596], seed=75, with_grad=True)
+    T = pool.h.shape[0]
+    W, h, tg, g = cuda(pool.W), cuda(pool.h), cuda(pool.targets), cuda(pool.g)
+    _, lse = rk.linear_logp(h, W, tg)
+    rk.set_row_blocks(blocks)
+    try:
+        dh_rounds = rk.linear_logp_bwd(h, W, tg, lse, g)
+        assert rk.last_tile_order("dh") == 2 and rk.last_row_blocks("dh") == blocks
+        ws = torch.empty(rk.linear_logp_bwd_workspace_size(T, H, V), dtype=torch.uint8,
+                         device=DEV)
+        dh = torch.empty((T, H), device=DEV)
+        cs = torch.cuda.Stream()
+        graph = _capture(lambda: rk.linear_logp_bwd(h, W, tg, lse, g, dh=dh, workspace=ws,
+                                                    stream=cs), cs)
+        assert rk.last_tile_order("dh") == 1
+    finally:
+        rk.set_row_blocks(0)
+    dh.fill_(float("nan"))
+    with torch.cuda.stream(cs):
+        graph.replay()
+    cs.synchronize()
+    assert same_bits(dh, dh_rounds)
+    assert rk.get_device_error() == 0

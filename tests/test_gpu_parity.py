@@ -350,8 +350,9 @@ def test_grpo_shape_sampled_rows(rk):
     logp, lse = rk.linear_logp(h, W, tg)
     dh = rk.linear_logp_bwd(h, W, tg, lse, g)
     # the launch the bench times: one pass over all rows, two row blocks per
-    # dh tile (K = 2004 stages of the vocabulary)
+    # dh tile (K = 2004 stages of the vocabulary), tiles taken in rounds
     assert rk.last_row_blocks("dh") == 2
+    assert rk.last_tile_order("dh") == 2
     rows = synth.sample_rows(lay.T, 64, seed=4)
     hb, Wb = bits_np(lay.h), bits_np(pool.W)
     ref_logp, ref_lse = oracle_linear(hb, Wb, lay.targets.numpy(), rows=rows)
