@@ -64,7 +64,6 @@ TRAFFIC_RECORD = {
     "source_sha1": "7c3e234d0aceff4780b66b6951b5ebf6f2817efb",
     "bytes_per_step": 104787588864,
     "per_launch_gb": {"fwd_saved": 37.16, "dh": 67.63},
-},
 }
 # Unique bytes a step has to move: forward h + W read, partials + target
 # logits + the softmax terms (T*V bf16) written; stash -> dZ pass: the terms
