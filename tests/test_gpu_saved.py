@@ -157,14 +157,16 @@ def _saved_terms(rk, saved, T, H, V):
     return saved[ws:ws + T * ld * 2].view(T, ld * 2)
 
 
-@pytest.mark.parametrize("all_pad", [False, True])
-def test_padding_blocks_are_skipped(rk, all_pad):
+@pytest.mark.parametrize("all_pad,H,V", [(False, 256, 3000), (True, 256, 3000),
+                                          (False, 2048, 16384)])
+def test_padding_blocks_are_skipped(rk, all_pad, H, V):
     # Sequences right-padded to 1024 rows: a block of 256 rows holding no
     # active row gets no tensor work.  Visible: the forward leaves the block's
     # saved terms as the buffer held them, and the backward writes dh = 0 there
     # over a NaN-filled output.  logp and lse are 0 there, and the active rows
-    # are the packed layout's bits.
-    H, V = 256, 3000
+    # are the packed layout's bits.  At V = 16384, H = 2048 the dh GEMM takes
+    # its 8 H tiles per row block in rounds (two rounds of the resident
+    # pairs), skipping the dead blocks' tiles within them.
     pool = synth.make_pool(H, V, [300, 40, 700, 129], seed=93, with_grad=True)
     seqs = [0, 1, 2, 3]
     lay = synth.padded(pool, seqs, 1024)
@@ -184,6 +186,8 @@ def test_padding_blocks_are_skipped(rk, all_pad):
         return lp.cpu(), lse.cpu(), dh.cpu(), terms.cpu()
 
     lp, lse, dh, terms = run(lay, 0xAB)
+    if V >= 16384 and not all_pad:
+        assert rk.last_tile_order("dh") == 2
     dead = (lay.targets.view(-1, 256) < 0).all(dim=1)
     assert int(dead.sum()) == (16 if all_pad else 9)
     for b in range(T // 256):
