@@ -40,16 +40,24 @@ def arch_key() -> str:
 class Runner:
     """Runs the three operators on a layout and extracts logical rows."""
 
-    def __init__(self, rk, pool, with_bwd=True, bwd_workspace=None):
+    def __init__(self, rk, pool, with_bwd=True, bwd_workspace=None, saved=False):
         self.rk = rk
         self.pool = pool
         self.W = cuda(pool.W)
         self.with_bwd = with_bwd and pool.g is not None
         self.bwd_workspace = bwd_workspace
+        self.saved = saved  # the forward that keeps its terms + the backward from them
 
     def run(self, lay):
         h, tg = cuda(lay.h), cuda(lay.targets)
         cu = cuda(lay.cu_seqlens)
+        if self.saved:
+            logp, lse, sv = self.rk.linear_logp_fwd_saved(h, self.W, tg, cu)
+            out = {"logp": logp, "lse": lse}
+            if self.with_bwd:
+                out["dh"] = self.rk.linear_logp_bwd_saved(h, self.W, tg, lse, cuda(lay.g), sv, cu)
+            torch.cuda.synchronize()
+            return {k: v.cpu() for k, v in out.items()}
         logp, lse = self.rk.linear_logp(h, self.W, tg, cu)
         out = {"logp": logp, "lse": lse}
         if self.with_bwd:
@@ -263,11 +271,14 @@ def test_llama_t1_t2_t3(rk):
 
 
 @pytest.mark.slow
-def test_qwen_padding_vs_packing(rk):
+@pytest.mark.parametrize("saved", [False, True])
+def test_qwen_padding_vs_packing(rk, saved):
     # logp, lse and dh of the active tokens, bitwise: B = 8 and B = 32
-    # right-padded, B = 1 padded, against the varlen pack (T4 / T6, T1)
+    # right-padded, B = 1 padded, against the varlen pack (T4 / T6, T1); with
+    # the recompute backward and with the saved-terms forward and backward
+    # (whose dh GEMM skips the padding blocks and takes its tiles in rounds)
     pool = synth.qwen_pool(with_grad=True)
-    runner = Runner(rk, pool)
+    runner = Runner(rk, pool, saved=saved)
     base = synth.packed(pool, list(range(8)))                    # varlen pack of seqs 0-7
     bout = runner.run(base)
     b8 = synth.padded(pool, list(range(8)), 2048)                # [8, 2048] right-padded
