@@ -347,3 +347,31 @@ def test_qwen_dw_padding_packing_permutation(rk):
         got = dw_of(lay, full).cpu()
         assert torch.equal(got.view(torch.int32), base.view(torch.int32)), (lay.description, full)
     assert rk.get_device_error() == 0
+
+
+@pytest.mark.slow
+def test_qwen_dw_saved_padding_packing_permutation(rk):
+    # The same sample set through the forward that keeps its softmax terms
+    # and rk_linear_logp_bwd_full_saved: dW (canonical order) and the active
+    # rows' dh bitwise equal across right- and left-padded batches and a
+    # permuted pack behind 37 pad rows.
+    pool = synth.qwen_pool(with_grad=True)
+    W = cuda(pool.W)
+    seqs = list(range(8))
+
+    def grads_of(lay):
+        order = torch.tensor([r for i in seqs for r in lay.rows_of[i]], dtype=torch.int64)
+        h, tg, g = cuda(lay.h), cuda(lay.targets), cuda(lay.g)
+        _, lse, saved = rk.linear_logp_fwd_saved(h, W, tg)
+        dh, dW = rk.linear_logp_bwd_full_saved(h, W, tg, lse, g, saved, row_order=cuda(order))
+        return dh[cuda(order)].cpu(), dW.cpu()
+
+    dh0, dw0 = grads_of(synth.packed(pool, seqs))
+    assert torch.isfinite(dw0).all() and torch.isfinite(dh0).all()
+    for lay in (synth.padded(pool, seqs, 2048, side="right"),
+                synth.padded(pool, seqs, 2048, side="left"),
+                synth.packed(pool, [7, 3, 5, 1, 0, 6, 2, 4], lead_pad=37)):
+        dh, dw = grads_of(lay)
+        assert torch.equal(dw.view(torch.int32), dw0.view(torch.int32)), lay.description
+        assert torch.equal(dh.view(torch.int32), dh0.view(torch.int32)), lay.description
+    assert rk.get_device_error() == 0
