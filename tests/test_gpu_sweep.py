@@ -1,0 +1,98 @@
+"""A seeded sweep of random shapes and masks against the oracle.
+
+Each case draws T, H and V (with V at and around the 8- and 256-column
+boundaries as well as in between), masks rows both by target (-100) and by
+cu_seqlens (leading and trailing rows outside the sequences), and checks:
+  - the forward against the oracle (|d logp| <= 1e-3 + 1e-3 |logp|, same for lse);
+  - the recompute backward and the saved-terms backward against the oracle
+    (|d dh| <= 1e-3 + 1e-3 max |dh|), and inactive rows exactly 0;
+  - the saved-terms forward and the forward with the GRPO loss give the plain
+    forward's logp and lse bits;
+  - on every fourth case, dW of the saved full backward against the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+from invariant_rl_logprob_gb300 import contract, synth
+from tests.helpers import cuda, bits_np, oracle_bwd, oracle_dw, oracle_linear, same_bits
+
+pytestmark = pytest.mark.gpu
+
+V_CHOICES = [1, 2, 7, 8, 9, 255, 256, 257, 511, 1000, 2049, 4095]
+
+
+@pytest.fixture(scope="module")
+def rk():
+    from invariant_rl_logprob_gb300 import build
+    build.build()
+    import invariant_rl_logprob_gb300 as m
+    m.load_library()
+    m.get_device_error()
+    return m
+
+
+def _case(i):
+    rng = np.random.default_rng(7000 + i)
+    T = int(rng.integers(1, 4)) if rng.random() < 0.3 else int(rng.integers(4, 400))
+    H = int(64 * rng.integers(1, 7))
+    V = int(V_CHOICES[i % len(V_CHOICES)] if i < len(V_CHOICES) else rng.integers(1, 4000))
+    lead = int(rng.integers(0, min(3, T - 1) + 1)) if T > 1 else 0
+    trail = int(rng.integers(0, min(3, T - 1 - lead) + 1)) if T - lead > 1 else 0
+    # sequence boundaries between lead and T - trail
+    inner = T - lead - trail
+    cuts = sorted(set(int(x) for x in rng.integers(1, max(inner, 2), size=3))) if inner > 2 else []
+    cu = [lead] + [lead + c for c in cuts if 0 < c < inner] + [lead + inner]
+    return T, H, V, np.array(cu, dtype=np.int32), rng
+
+
+@pytest.mark.parametrize("i", range(48))
+def test_random_shape_and_mask_vs_oracle(rk, i):
+    T, H, V, cu, rng = _case(i)
+    gen = synth.generator(9100 + i)
+    W = synth.normal_bf16(gen, (V, H), 0.05)
+    h = synth.normal_bf16(gen, (T, H), 1.0)
+    tg = synth.uniform_targets(gen, T, V)
+    drop = rng.random(T) < 0.1
+    tg[torch.as_tensor(drop)] = -100
+    g = torch.randn(T, generator=gen, dtype=torch.float32)
+    hd, Wd, tgd, gd = cuda(h), cuda(W), cuda(tg), cuda(g)
+    cud = cuda(torch.as_tensor(cu))
+    desc = f"T={T} H={H} V={V} cu={cu.tolist()}"
+
+    logp, lse = rk.linear_logp(hd, Wd, tgd, cud)
+    hb, Wb = bits_np(h), bits_np(W)
+    ref_lp, ref_lse = oracle_linear(hb, Wb, tg.numpy(), cu)
+    for got, ref, name in ((logp, ref_lp, "logp"), (lse, ref_lse, "lse")):
+        err = np.abs(got.cpu().double().numpy() - ref)
+        assert np.all(err <= 1e-3 + 1e-3 * np.abs(ref)), (desc, name, float(err.max()))
+
+    ref_dh = oracle_bwd(hb, Wb, tg.numpy(), g.double().numpy(), cu)
+    inactive = np.ones(T, dtype=bool)
+    inactive[cu[0]:cu[-1]] = False
+    inactive |= tg.numpy() < 0
+    dh = rk.linear_logp_bwd(hd, Wd, tgd, lse, gd, cud)
+    chk = contract.check_gradient_accuracy(dh.cpu().numpy(), ref_dh)
+    assert chk.passed, (desc, "recompute", chk)
+
+    lp_s, lse_s, saved = rk.linear_logp_fwd_saved(hd, Wd, tgd, cud)
+    assert same_bits(lp_s, logp) and same_bits(lse_s, lse), desc
+    dh_s = rk.linear_logp_bwd_saved(hd, Wd, tgd, lse_s, gd, saved, cud)
+    chk = contract.check_gradient_accuracy(dh_s.cpu().numpy(), ref_dh)
+    assert chk.passed, (desc, "saved", chk)
+    for d in (dh, dh_s):
+        assert bool((d.cpu()[torch.as_tensor(inactive)] == 0).all()), desc
+
+    # the forward with the per-token GRPO loss in its merge: same logp / lse
+    old = logp + 0.05 * torch.randn(T, device=logp.device)
+    adv = torch.randn(T, device=logp.device)
+    out = rk.linear_logp_grpo(hd, Wd, tgd, old, adv, cu_seqlens=cud)
+    assert same_bits(out["logp"], logp) and same_bits(out["lse"], lse), desc
+
+    if i % 4 == 0:
+        _, lse_f, saved_f = rk.linear_logp_fwd_saved(hd, Wd, tgd, cud)
+        _, dW = rk.linear_logp_bwd_full_saved(hd, Wd, tgd, lse_f, gd, saved_f, cud)
+        ref_dw = oracle_dw(hb, Wb, tg.numpy(), g.double().numpy(), cu)
+        chk = contract.check_gradient_accuracy(dW.cpu().numpy(), ref_dw)
+        assert chk.passed, (desc, "dW", chk)
+    assert rk.get_device_error() == 0
