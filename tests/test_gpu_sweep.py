@@ -96,3 +96,36 @@ def test_random_shape_and_mask_vs_oracle(rk, i):
         chk = contract.check_gradient_accuracy(dW.cpu().numpy(), ref_dw)
         assert chk.passed, (desc, "dW", chk)
     assert rk.get_device_error() == 0
+
+
+LOGITS_V = [1, 2, 7, 8, 9, 63, 64, 65, 255, 256, 257, 1000, 8191, 8192, 8193, 32000, 100003]
+
+
+@pytest.mark.parametrize("i", range(len(LOGITS_V)))
+def test_random_logits_path_vs_oracle(rk, i):
+    # the logits path and its backward on random shapes and masks, V across
+    # the 8-value group and the 64-value batch boundaries of the row kernel
+    import oracle
+    V = LOGITS_V[i]
+    rng = np.random.default_rng(7500 + i)
+    T = int(rng.integers(1, 300))
+    gen = synth.generator(9500 + i)
+    z = (torch.randn((T, V), generator=gen) * 2.0).to(torch.bfloat16)
+    tg = synth.uniform_targets(gen, T, V)
+    tg[torch.as_tensor(rng.random(T) < 0.1)] = -100
+    lead = int(rng.integers(0, min(3, T) + 1))
+    cu = np.array([lead, max(lead, T - int(rng.integers(0, 3)))], dtype=np.int32)
+    g = torch.randn(T, generator=gen, dtype=torch.float32)
+    zd, tgd, cud, gd = cuda(z), cuda(tg), cuda(torch.as_tensor(cu)), cuda(g)
+    desc = f"T={T} V={V} cu={cu.tolist()}"
+    logp, lse = rk.logp_from_logits(zd, tgd, cud)
+    zb = bits_np(z)
+    ref_lp, ref_lse = oracle.logp_from_logits(zb, tg.numpy(), cu)
+    for got, ref, name in ((logp, ref_lp, "logp"), (lse, ref_lse, "lse")):
+        err = np.abs(got.cpu().double().numpy() - ref)
+        assert np.all(err <= 1e-3 + 1e-3 * np.abs(ref)), (desc, name, float(err.max()))
+    dz = rk.logp_from_logits_bwd(zd, tgd, lse, gd, cud)
+    ref_dz = oracle.logits_bwd(zb, tg.numpy(), g.double().numpy(), cu)
+    chk = contract.check_gradient_accuracy(dz.cpu().numpy(), ref_dz)
+    assert chk.passed, (desc, chk)
+    assert rk.get_device_error() == 0
