@@ -129,3 +129,41 @@ def test_random_logits_path_vs_oracle(rk, i):
     chk = contract.check_gradient_accuracy(dz.cpu().numpy(), ref_dz)
     assert chk.passed, (desc, chk)
     assert rk.get_device_error() == 0
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_lm_head_and_greedy_vs_oracle(rk, i):
+    # the dense path's bf16 logits and the greedy step on random shapes:
+    #  - lm_head within one bf16 rounding of the fp32 accumulation, whose own
+    #    error is bounded by z_error_bound;
+    #  - the greedy token within the bounds of the maximum, the oracle's
+    #    argmax wherever it is unambiguous, and logp of the chosen token
+    import oracle
+    from tests.helpers import oracle_lm_head, z_error_bound
+    rng = np.random.default_rng(7700 + i)
+    T = int(rng.integers(1, 300))
+    H = int(64 * rng.integers(1, 9))
+    V = int(V_CHOICES[i] if i < len(V_CHOICES) else rng.integers(1, 5000))
+    gen = synth.generator(9700 + i)
+    W = synth.normal_bf16(gen, (V, H), 0.05)
+    h = synth.normal_bf16(gen, (T, H), 1.0)
+    hd, Wd = cuda(h), cuda(W)
+    hb, Wb = bits_np(h), bits_np(W)
+    desc = f"T={T} H={H} V={V}"
+    ref = oracle_lm_head(hb, Wb, list(range(T)))
+    acc = z_error_bound(hb, Wb, list(range(T)))
+    z = rk.lm_head(hd, Wd).float().cpu().numpy()
+    assert np.all(np.abs(z - ref) <= 2.0 ** -8 * (np.abs(ref) + acc) + acc), desc
+    tok, lp, _ = rk.linear_greedy(hd, Wd)
+    j = tok.cpu().numpy()
+    r = np.arange(T)
+    a = ref.argmax(axis=1)
+    assert np.all(ref[r, j] >= ref[r, a] - acc[r, j] - acc[r, a]), desc
+    hi = ref + acc
+    hi[r, a] = -np.inf
+    clear = (ref[r, a] - acc[r, a]) > hi.max(axis=1)
+    assert np.all(j[clear] == a[clear]), desc
+    ref_lp, _ = oracle.linear_logp(hb, Wb, j)
+    err = np.abs(lp.cpu().double().numpy() - ref_lp)
+    assert np.all(err <= 1e-3 + 1e-3 * np.abs(ref_lp)), (desc, float(err.max()))
+    assert rk.get_device_error() == 0
