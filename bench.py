@@ -200,14 +200,27 @@ def make_inputs(rank: int):
     return pool, logits
 
 
-def cpu_oracle_sample(pool, logits, n_rows: int) -> tuple[float, int, str]:
-    """Time the fp64 oracle (single thread) on n_rows GRPO rows (fwd + bwd) and
-    n_rows logits-path rows; returns (tokens/s, cores, description)."""
-    import numpy as np
+def oracle_threads() -> int:
+    """Host cores the oracle runs on (threads over rows; its C calls release
+    the GIL, and every row is computed independently)."""
+    try:
+        n = len(os.sched_getaffinity(0))  # the CPUs this process may run on
+    except (AttributeError, OSError):
+        n = os.cpu_count() or 1
+    return max(1, n)
+
+
+def cpu_oracle_sample(pool, logits, rows_per_thread: int) -> tuple[float, int, str]:
+    """Time the fp64 oracle, unchanged, on the host cores: each of `threads`
+    threads takes rows_per_thread GRPO rows (fwd + bwd) and as many
+    logits-path rows; returns (tokens/s, threads, description)."""
+    import concurrent.futures as cf
 
     import oracle
     from invariant_rl_logprob_gb300 import synth
     oracle.build()
+    threads = oracle_threads()
+    n_rows = rows_per_thread * threads
     hb = synth.bf16_bits(pool.h)
     Wb = synth.bf16_bits(pool.W)
     tg = pool.targets.numpy()
@@ -215,17 +228,24 @@ def cpu_oracle_sample(pool, logits, n_rows: int) -> tuple[float, int, str]:
     rows = synth.sample_rows(pool.h.shape[0], n_rows, seed=4)
     zb = synth.bf16_bits(logits[0][0])
     ztg = logits[0][1].numpy()
-    zrows = synth.sample_rows(zb.shape[0], n_rows, seed=1)
+    zrows = synth.sample_rows(zb.shape[0], min(n_rows, zb.shape[0]), seed=1)
+
+    def work(k):
+        rr = rows[k::threads]
+        oracle.linear_logp(hb, Wb, tg, rows=rr)
+        oracle.linear_logp_bwd(hb, Wb, tg, g, rows=rr)
+        oracle.logp_from_logits(zb, ztg, rows=zrows[k::threads])
+
     t0 = time.perf_counter()
-    oracle.linear_logp(hb, Wb, tg, rows=rows)
-    oracle.linear_logp_bwd(hb, Wb, tg, g, rows=rows)
-    oracle.logp_from_logits(zb, ztg, rows=zrows)
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(work, range(threads)))
     dt = time.perf_counter() - t0
     # one GRPO row of the step carries 2048/65536 of a logits-path row with it;
     # the logits rows are timed in full and charged to the same token count
-    desc = (f"{n_rows} GRPO rows (fwd + bwd, H=4096, V=128256) + {n_rows} logits-path rows "
-            f"(V=32000), fp64 oracle, 1 thread, {dt:.1f} s")
-    return n_rows / dt, 1, desc
+    desc = (f"{n_rows} GRPO rows (fwd + bwd, H=4096, V=128256) + {len(zrows)} logits-path rows "
+            f"(V=32000), fp64 oracle, {threads} threads (one per host core, rows split "
+            f"between them), {dt:.1f} s")
+    return n_rows / dt, threads, desc
 
 
 def run_reference(args) -> None:
@@ -239,10 +259,10 @@ def run_reference(args) -> None:
     pool = synth.make_pool(GRPO["H"], GRPO["V"], lengths, c["seed"], with_grad=True)
     z, ztg, _ = synth.logits_batch()
     logits = [(z, ztg)]
-    rows_per_step = 1
+    rows_per_step = oracle_threads()   # one row per host core per step
     times = []
     for i in range(args.warmup + args.steps):
-        v, cores, desc = cpu_oracle_sample(pool, logits, rows_per_step)
+        v, cores, desc = cpu_oracle_sample(pool, logits, 1)
         if i >= args.warmup:
             times.append(rows_per_step / v)
     ms = 1000.0 * statistics.mean(times)
@@ -253,7 +273,7 @@ def run_reference(args) -> None:
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample": f"{rows_per_step} GRPO row(s) fwd+bwd + "
                    f"{rows_per_step} logits-path row(s) per step"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -924,7 +944,8 @@ def main() -> None:
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=8)
+    ap.add_argument("--cpu-rows", type=int, default=2,
+                    help="GRPO rows (and logits-path rows) per host core in the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the separate timing of the widened rows")
