@@ -671,6 +671,7 @@ def run_gpu(args) -> None:
     lg_us = sorted(r["us_per_call"] for r in lg_runs)
     lg_loop_ms = statistics.median(lg_us) / 1000.0
 
+    dh_order = rk.last_tile_order("dh")
     ms_step_local = total_ms / args.steps
     ms_step = max_over_ranks(ms_step_local, ws)
     value = ws * T / (ms_step / 1000.0)
@@ -837,6 +838,8 @@ def run_gpu(args) -> None:
                        "host copies of its dh/logp, each direction on its own stream, "
                        "double-buffered against the compute stream; timed from the first "
                        "copy to the last"},
+        "dh_tile_order": {2: "rounds (cooperative launch)", 1: "tiles from a counter"}.get(
+            dh_order, "none"),
         "gpu_launches": launches_per_step * args.steps,
         "gpu_launches_note": f"{launches_per_step} librk kernels per step x {args.steps} steps "
                              "in the timed region",

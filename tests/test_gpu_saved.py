@@ -187,7 +187,7 @@ def test_padding_blocks_are_skipped(rk, all_pad, H, V):
 
     lp, lse, dh, terms = run(lay, 0xAB)
     if V >= 16384 and not all_pad:
-        assert rk.last_tile_order("dh") == 2
+        assert rk.last_tile_order("dh") in (1, 2)  # 2: rounds, unless refused
     dead = (lay.targets.view(-1, 256) < 0).all(dim=1)
     assert int(dead.sum()) == (16 if all_pad else 9)
     for b in range(T // 256):
