@@ -131,8 +131,9 @@ rk_status rk_logp_from_logits(const uint16_t *logits, const int64_t *targets,
 
 /*
  * Bytes of workspace rk_linear_logp_bwd needs to process all T rows in one
- * pass (one bf16 [T, V] buffer of g * softmax probabilities, rounded up, and
- * 256 bytes for a tile counter).
+ * pass (one bf16 [T, V] buffer of g * softmax probabilities, rounded up, the
+ * rows' fp32 entry lists, a flag per 256-row block and 256 bytes for the
+ * tile and round counters).
  * A smaller workspace (but at least rk_linear_logp_bwd_min_workspace_size)
  * makes the call process the rows in chunks; the results do not change.
  */
