@@ -863,7 +863,21 @@ def run_case(args) -> None:
     rk_build.build()
     dev = torch.device("cuda", 0)
     T, H, V = (int(x) for x in args.shape.split(","))
-    if args.case in ("logits", "logits_bwd"):
+    if args.case in ("qwen_padded", "qwen_packed"):
+        # the Qwen-shaped forward on sequences 0-7: [8, 2048] right-padded
+        # (256-row blocks of padding skipped) or varlen-packed
+        pool = synth.qwen_pool()
+        seqs = list(range(8))
+        lay = (synth.padded(pool, seqs, 2048) if args.case == "qwen_padded"
+               else synth.packed(pool, seqs))
+        W = pool.W.to(dev)
+        h, tg = lay.h.to(dev), lay.targets.to(dev)
+        cu = lay.cu_seqlens.to(dev) if lay.cu_seqlens is not None else None
+        T, H, V = h.shape[0], h.shape[1], W.shape[0]
+        fn = lambda: rk.linear_logp(h, W, tg, cu)
+        n_act = sum(len(lay.rows_of[i]) for i in seqs)
+        work = f"{2.0 * n_act * H * V / 1e12:.3f} TFLOP on {n_act} active of {T} rows"
+    elif args.case in ("logits", "logits_bwd"):
         z, tg, _ = synth.logits_batch(T=T, V=V)
         z, tg = z.to(dev), tg.to(dev)
         if args.case == "logits":
@@ -953,6 +967,7 @@ def main() -> None:
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the separate timing of the widened rows")
     ap.add_argument("--case", choices=["fwd", "bwd", "logits", "logits_bwd", "dw", "full", "saved",
+                                       "qwen_padded", "qwen_packed",
                                        "full_saved"],
                     default=None)
     ap.add_argument("--shape", default="2048,4096,32000")
