@@ -1189,6 +1189,8 @@ cudaError_t run_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tile
     const int64_t tiles =
         (int64_t)((a.num_m + TileCfg<MODE>::kMB - 1) / TileCfg<MODE>::kMB) * a.num_n;
     if (tiles == 0) return cudaSuccess;
+    // tile numbers travel as int32 (the queue slots and the counters)
+    if (tiles > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
     const int64_t pairs = std::min<int64_t>(tiles, resident_pairs<MODE>(di));
     const unsigned grid = (unsigned)(2 * pairs);
     CUtensorMap unused;
