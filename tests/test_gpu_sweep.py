@@ -167,3 +167,48 @@ def test_random_lm_head_and_greedy_vs_oracle(rk, i):
     err = np.abs(lp.cpu().double().numpy() - ref_lp)
     assert np.all(err <= 1e-3 + 1e-3 * np.abs(ref_lp)), (desc, float(err.max()))
     assert rk.get_device_error() == 0
+
+
+@pytest.mark.parametrize("i", range(40))
+def test_random_layout_invariance(rk, i):
+    # a random pool of sequences in random layouts (packed, permuted behind
+    # random lead padding, right- and left-padded to the longest, a random
+    # subset packed): every active row's logp, lse and dh, from both the
+    # recompute and the saved-terms backward, bitwise equal to the packed
+    # layout's
+    rng = np.random.default_rng(7900 + i)
+    H = int(64 * rng.integers(1, 7))
+    V = int(rng.choice([7, 256, 257, 1000, 3001, 16384]))
+    n = int(rng.integers(1, 7))
+    lengths = [int(x) for x in rng.integers(1, 600, size=n)]
+    pool = synth.make_pool(H, V, lengths, seed=9900 + i, with_grad=True)
+    W = cuda(pool.W)
+    seqs = list(range(n))
+
+    def run(lay):
+        h, tg, g = cuda(lay.h), cuda(lay.targets), cuda(lay.g)
+        cu = cuda(lay.cu_seqlens)
+        logp, lse = rk.linear_logp(h, W, tg, cu)
+        dh = rk.linear_logp_bwd(h, W, tg, lse, g, cu)
+        lp_s, lse_s, saved = rk.linear_logp_fwd_saved(h, W, tg, cu)
+        dh_s = rk.linear_logp_bwd_saved(h, W, tg, lse_s, g, saved, cu)
+        return {"logp": logp.cpu(), "lse": lse.cpu(), "dh": dh.cpu(), "logp_s": lp_s.cpu(),
+                "dh_s": dh_s.cpu()}
+
+    base = synth.packed(pool, seqs)
+    bout = run(base)
+    perm = [int(x) for x in rng.permutation(n)]
+    sub = sorted(int(x) for x in rng.choice(n, size=int(rng.integers(1, n + 1)), replace=False))
+    longest = max(lengths)
+    layouts = [(synth.packed(pool, perm, lead_pad=int(rng.integers(0, 300))), seqs),
+               (synth.padded(pool, seqs, longest, side="right"), seqs),
+               (synth.padded(pool, seqs, longest + int(rng.integers(0, 40)), side="left"), seqs),
+               (synth.packed(pool, sub), sub)]
+    for lay, ids in layouts:
+        out = run(lay)
+        for s_id in ids:
+            a, b = lay.rows_of[s_id], base.rows_of[s_id]
+            for k in out:
+                assert torch.equal(out[k][a].view(torch.int32), bout[k][b].view(torch.int32)), \
+                    (k, lay.description, s_id)
+    assert rk.get_device_error() == 0
