@@ -211,4 +211,25 @@ def test_random_layout_invariance(rk, i):
             for k in out:
                 assert torch.equal(out[k][a].view(torch.int32), bout[k][b].view(torch.int32)), \
                     (k, lay.description, s_id)
+
+    # dW over the whole sample set, named in canonical (sequence, position)
+    # order: the same bits from every layout that holds all sequences, from
+    # rk_linear_logp_dw and from the saved full backward
+    def dw_of(lay):
+        order = cuda(torch.tensor([r for s_id in seqs for r in lay.rows_of[s_id]],
+                                  dtype=torch.int64))
+        h, tg, g = cuda(lay.h), cuda(lay.targets), cuda(lay.g)
+        cu = cuda(lay.cu_seqlens)
+        _, lse = rk.linear_logp(h, W, tg, cu)
+        dw = rk.linear_logp_dw(h, W, tg, lse, g, cu, row_order=order).cpu()
+        _, lse_s, saved = rk.linear_logp_fwd_saved(h, W, tg, cu)
+        dw_s = rk.linear_logp_bwd_full_saved(h, W, tg, lse_s, g, saved, cu, row_order=order)[1]
+        return dw, dw_s.cpu()
+
+    if i % 2 == 0:
+        dw0, dws0 = dw_of(base)
+        for lay, ids in layouts[:3]:
+            dw, dws = dw_of(lay)
+            assert torch.equal(dw.view(torch.int32), dw0.view(torch.int32)), lay.description
+            assert torch.equal(dws.view(torch.int32), dws0.view(torch.int32)), lay.description
     assert rk.get_device_error() == 0
