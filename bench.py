@@ -829,8 +829,10 @@ def run_gpu(args) -> None:
                                   "on the device before and after each loop",
                         "in_step": {"us_per_call": lg_ms * 1000.0, "achieved": lg_gbs_step,
                                     "frac": lg_gbs_step / peaks["hbm_gbs"],
-                                    "note": "measured right after the dh GEMM: its dirty L2 "
-                                            "lines are written back during this call"}},
+                                    "note": "one call between two events in each step, right "
+                                            "after the backward call (at the clock the power-"
+                                            "capped GEMMs leave, and with no neighbouring call "
+                                            "to hide its launch)"}},
         "rows": rows,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
