@@ -679,10 +679,11 @@ def run_gpu(args) -> None:
 
     # ---- end to end: host buffers in, results out, through the public API ----
     # Every step copies its inputs from pinned host memory and its results
-    # back.  Two device buffer sets let step i+1's inputs (host-to-device
+    # back.  Three device buffer sets: step i+2's inputs (host-to-device
     # stream) and step i-1's results (device-to-host stream) move while step i
-    # computes.  (With one stream for both directions the loop stalled for
-    # 12-24 ms every few steps.)
+    # computes, so each copy has two steps to finish.  (With one stream for
+    # both directions the loop stalled for 12-24 ms every few steps; with two
+    # sets, a single copy slowed by the shared host stalled it by up to 42 ms.)
     pin = lambda t: t.pin_memory()
     h_h, W_h, tg_h, g_h = pin(pool.h), pin(pool.W), pin(pool.targets), pin(pool.g)
     z_h = [(pin(z), pin(t)) for z, t in logits_host]
@@ -694,11 +695,13 @@ def run_gpu(args) -> None:
     d2h = dh_h.numel() * 4 + logp_h.numel() * 4 + zlogp_h.numel() * 4
     sets = [dict(h=h, W=W, tg=tg, g=g, z=zs[0][0], zt=zs[0][1], logp=logp, lse=lse, dh=dh,
                  zlogp=zlogp, zlse=zlse)]
-    sets.append(dict(h=torch.empty_like(h), W=torch.empty_like(W), tg=torch.empty_like(tg),
-                     g=torch.empty_like(g), z=torch.empty_like(zs[0][0]),
-                     zt=torch.empty_like(zs[0][1]), logp=torch.empty_like(logp),
-                     lse=torch.empty_like(lse), dh=torch.empty_like(dh),
-                     zlogp=torch.empty_like(zlogp), zlse=torch.empty_like(zlse)))
+    n_sets = 3
+    for _ in range(n_sets - 1):
+        sets.append(dict(h=torch.empty_like(h), W=torch.empty_like(W), tg=torch.empty_like(tg),
+                         g=torch.empty_like(g), z=torch.empty_like(zs[0][0]),
+                         zt=torch.empty_like(zs[0][1]), logp=torch.empty_like(logp),
+                         lse=torch.empty_like(lse), dh=torch.empty_like(dh),
+                         zlogp=torch.empty_like(zlogp), zlse=torch.empty_like(zlse)))
     in_stream = torch.cuda.Stream(dev)
     out_stream = torch.cuda.Stream(dev)
 
@@ -724,29 +727,31 @@ def run_gpu(args) -> None:
         zlogp_h.copy_(b["zlogp"], non_blocking=True)
 
     def e2e_run(n_steps):
-        in_ready = [torch.cuda.Event() for _ in range(2)]
-        done = [torch.cuda.Event() for _ in range(2)]
-        out_read = [torch.cuda.Event() for _ in range(2)]
+        in_ready = [torch.cuda.Event() for _ in range(n_sets)]
+        done = [torch.cuda.Event() for _ in range(n_sets)]
+        out_read = [torch.cuda.Event() for _ in range(n_sets)]
         with torch.cuda.stream(in_stream):
-            h2d_into(sets[0], 0)
-            in_ready[0].record(in_stream)
+            for j in range(min(n_sets - 1, n_steps)):  # the first steps' inputs
+                h2d_into(sets[j], j)
+                in_ready[j].record(in_stream)
         for i in range(n_steps):
-            b, nb_ = sets[i % 2], sets[(i + 1) % 2]
-            stream.wait_event(in_ready[i % 2])
-            if i >= 2:
-                stream.wait_event(out_read[i % 2])    # results of step i-2 read out
+            b = sets[i % n_sets]
+            stream.wait_event(in_ready[i % n_sets])
+            if i >= n_sets:
+                stream.wait_event(out_read[i % n_sets])    # step i-3's results read out
             compute(b)
-            done[i % 2].record(stream)
-            if i + 1 < n_steps:
+            done[i % n_sets].record(stream)
+            k = i + n_sets - 1  # the step whose inputs go in now
+            if k < n_steps:
                 with torch.cuda.stream(in_stream):
-                    if i >= 1:
-                        in_stream.wait_event(done[(i + 1) % 2])   # step i-1 done with nb_
-                    h2d_into(nb_, i + 1)
-                    in_ready[(i + 1) % 2].record(in_stream)
+                    if k >= n_sets:
+                        in_stream.wait_event(done[k % n_sets])  # step k-3 done with the set
+                    h2d_into(sets[k % n_sets], k)
+                    in_ready[k % n_sets].record(in_stream)
             with torch.cuda.stream(out_stream):
-                out_stream.wait_event(done[i % 2])
+                out_stream.wait_event(done[i % n_sets])
                 d2h_from(b)
-                out_read[i % 2].record(out_stream)
+                out_read[i % n_sets].record(out_stream)
         stream.wait_stream(in_stream)
         stream.wait_stream(out_stream)
 
@@ -839,7 +844,8 @@ def run_gpu(args) -> None:
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "how": "pinned host -> device copies of every step's inputs and device -> "
                        "host copies of its dh/logp, each direction on its own stream, "
-                       "double-buffered against the compute stream; timed from the first "
+                       "three buffer sets against the compute stream (each copy has two "
+                       "steps to finish); timed from the first "
                        "copy to the last"},
         "dh_tile_order": {2: "rounds (cooperative launch)", 1: "tiles from a counter"}.get(
             dh_order, "none"),
