@@ -679,11 +679,13 @@ def run_gpu(args) -> None:
 
     # ---- end to end: host buffers in, results out, through the public API ----
     # Every step copies its inputs from pinned host memory and its results
-    # back.  Three device buffer sets: step i+2's inputs (host-to-device
-    # stream) and step i-1's results (device-to-host stream) move while step i
-    # computes, so each copy has two steps to finish.  (With one stream for
-    # both directions the loop stalled for 12-24 ms every few steps; with two
-    # sets, a single copy slowed by the shared host stalled it by up to 42 ms.)
+    # back.  Four device buffer sets: the inputs of step i+3 (host-to-device
+    # stream) and the results of step i-1 (device-to-host stream) move while
+    # step i computes, so each copy has three steps to finish.  Events around
+    # every copy showed single copies slowed by the shared host from 6-9 ms to
+    # 65-150 ms, once or twice a run; with two sets such a copy stalled the
+    # loop by up to 42 ms.  (With one stream for both directions the loop
+    # stalled for 12-24 ms every few steps.)
     pin = lambda t: t.pin_memory()
     h_h, W_h, tg_h, g_h = pin(pool.h), pin(pool.W), pin(pool.targets), pin(pool.g)
     z_h = [(pin(z), pin(t)) for z, t in logits_host]
@@ -695,7 +697,7 @@ def run_gpu(args) -> None:
     d2h = dh_h.numel() * 4 + logp_h.numel() * 4 + zlogp_h.numel() * 4
     sets = [dict(h=h, W=W, tg=tg, g=g, z=zs[0][0], zt=zs[0][1], logp=logp, lse=lse, dh=dh,
                  zlogp=zlogp, zlse=zlse)]
-    n_sets = 3
+    n_sets = 4
     for _ in range(n_sets - 1):
         sets.append(dict(h=torch.empty_like(h), W=torch.empty_like(W), tg=torch.empty_like(tg),
                          g=torch.empty_like(g), z=torch.empty_like(zs[0][0]),
@@ -738,14 +740,14 @@ def run_gpu(args) -> None:
             b = sets[i % n_sets]
             stream.wait_event(in_ready[i % n_sets])
             if i >= n_sets:
-                stream.wait_event(out_read[i % n_sets])    # step i-3's results read out
+                stream.wait_event(out_read[i % n_sets])    # step i-n_sets's results read out
             compute(b)
             done[i % n_sets].record(stream)
             k = i + n_sets - 1  # the step whose inputs go in now
             if k < n_steps:
                 with torch.cuda.stream(in_stream):
                     if k >= n_sets:
-                        in_stream.wait_event(done[k % n_sets])  # step k-3 done with the set
+                        in_stream.wait_event(done[k % n_sets])  # step k-n_sets done with the set
                     h2d_into(sets[k % n_sets], k)
                     in_ready[k % n_sets].record(in_stream)
             with torch.cuda.stream(out_stream):
@@ -844,7 +846,7 @@ def run_gpu(args) -> None:
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "how": "pinned host -> device copies of every step's inputs and device -> "
                        "host copies of its dh/logp, each direction on its own stream, "
-                       "three buffer sets against the compute stream (each copy has two "
+                       "four buffer sets against the compute stream (each copy has three "
                        "steps to finish); timed from the first "
                        "copy to the last"},
         "dh_tile_order": {2: "rounds (cooperative launch)", 1: "tiles from a counter"}.get(
