@@ -748,17 +748,29 @@ def run_gpu(args) -> None:
                 with torch.cuda.stream(in_stream):
                     if k >= n_sets:
                         in_stream.wait_event(done[k % n_sets])  # step k-n_sets done with the set
+                    c0 = torch.cuda.Event(enable_timing=True)
+                    c0.record(in_stream)
                     h2d_into(sets[k % n_sets], k)
+                    c1 = torch.cuda.Event(enable_timing=True)
+                    c1.record(in_stream)
+                    copy_ev["h2d"].append((c0, c1))
                     in_ready[k % n_sets].record(in_stream)
             with torch.cuda.stream(out_stream):
                 out_stream.wait_event(done[i % n_sets])
+                c0 = torch.cuda.Event(enable_timing=True)
+                c0.record(out_stream)
                 d2h_from(b)
+                c1 = torch.cuda.Event(enable_timing=True)
+                c1.record(out_stream)
+                copy_ev["d2h"].append((c0, c1))
                 out_read[i % n_sets].record(out_stream)
         stream.wait_stream(in_stream)
         stream.wait_stream(out_stream)
 
+    copy_ev = {"h2d": [], "d2h": []}  # per-copy events (the copies' own durations)
     e2e_run(2)
     torch.cuda.synchronize(dev)
+    copy_ev = {"h2d": [], "d2h": []}
     barrier(ws)
     s2 = torch.cuda.Event(enable_timing=True)
     e2 = torch.cuda.Event(enable_timing=True)
@@ -768,6 +780,11 @@ def run_gpu(args) -> None:
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(s2.elapsed_time(e2) / args.steps, ws)
     e2e_value = ws * T / (e2e_ms / 1000.0)
+    copy_ms = {}
+    for key, evs in copy_ev.items():
+        d = sorted(a.elapsed_time(b) for a, b in evs)
+        if d:
+            copy_ms[key] = {"median": statistics.median(d), "max": d[-1], "n": len(d)}
     err = rk.get_device_error(stream)
     if err:
         raise RuntimeError(f"device error word {err:#x} in the end-to-end loop")
@@ -843,7 +860,7 @@ def run_gpu(args) -> None:
         "rows": rows,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "copy_ms": copy_ms,
                 "how": "pinned host -> device copies of every step's inputs and device -> "
                        "host copies of its dh/logp, each direction on its own stream, "
                        "four buffer sets against the compute stream (each copy has three "
