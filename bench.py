@@ -17,17 +17,22 @@ device time, inputs resident in HBM.  h (512 MB) and W (1.05 GB) exceed the
 126 MB L2, so nothing carries over between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-    python bench.py --case {fwd,bwd,dw,full,saved,full_saved,logits,logits_bwd} [--shape T,H,V]
-                        [--reps R]
+    python bench.py --case {fwd,bwd,dw,full,saved,full_saved,logits,logits_bwd,
+                            qwen_padded,qwen_packed} [--shape T,H,V] [--reps R]
 
 `--case` runs one operator a few times on a small workload (for profiler
 captures; default T=2048, H=4096, V=32000: W and the logits exceed L2) and
-prints its mean device time.
+prints its mean device time.  qwen_padded / qwen_packed run the Qwen-shaped
+forward on sequences 0-7, right-padded to [8, 2048] or varlen-packed.
 
 Under torchrun (N > 1) every rank runs its own group (weak scaling, no data
 collective); the timed region is bracketed by barriers and the max over ranks
 is reported.  `--impl reference` times the fp64 CPU oracle on a bounded sample
-of the same workload instead (rank 0 only).
+of the same workload instead (rank 0 only, one thread per host CPU).
+
+The end-to-end figure (`e2e`) runs the same step from pinned host buffers:
+every step's inputs are copied in and its dh / logp copied out, on their own
+streams, against four device buffer sets.
 """
 from __future__ import annotations
 
